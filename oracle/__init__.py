@@ -1,0 +1,4 @@
+"""fp64 CPU oracle (test infrastructure only; see lce_oracle's header)."""
+from .lce_oracle import (  # noqa: F401
+    forward, forward_backward, lse_rows, out_of_range_targets, sampled_reference, valid_rows,
+)

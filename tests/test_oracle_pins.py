@@ -1,0 +1,275 @@
+"""Pins for the fp64 oracle against facts fixed by the definition and by
+mathematics, not by the oracle itself: closed forms, a hand-derived worked
+example, central finite differences, an independent library autograd, and
+invariants. Each is chosen so that a plausible slip in the oracle (a dropped
+-onehot term, the wrong normaliser, a transposed operand, a wrong index or sign)
+fails at least one of them."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from synth_inputs import IGNORE_INDEX
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand(N, d, V, seed=0, pad=0.25, scale=1.0):
+    g = np.random.default_rng(seed)
+    H = g.standard_normal((N, d))
+    W = g.standard_normal((V, d)) * scale
+    t = g.integers(0, V, N)
+    t[g.random(N) < pad] = IGNORE_INDEX
+    return H, W, t
+
+
+# ---------------------------------------------------------------- closed forms
+
+def test_zero_W_gives_ln_V_and_closed_form_dW():
+    H, _, t = _rand(37, 5, 11, seed=1)
+    W = np.zeros((11, 5))
+    r = oracle.forward_backward(H, W, t)
+    valid = t != IGNORE_INDEX
+    nv = valid.sum()
+    assert r["loss"] == pytest.approx(math.log(11), abs=1e-14)
+    # every logit is 0, p = 1/V: dW_v = (1/(V Nv)) sum_i H_i - (1/Nv) sum_{i: t_i = v} H_i
+    expect = np.tile(H[valid].sum(0) / (11 * nv), (11, 1))
+    for i in np.nonzero(valid)[0]:
+        expect[t[i]] -= H[i] / nv
+    np.testing.assert_allclose(r["dW"], expect, atol=1e-14)
+    np.testing.assert_array_equal(r["dH"], 0.0)
+
+
+def test_zero_H_gives_ln_V_and_closed_form_dH():
+    _, W, t = _rand(29, 4, 7, seed=2)
+    H = np.zeros((29, 4))
+    r = oracle.forward_backward(H, W, t)
+    valid = t != IGNORE_INDEX
+    nv = valid.sum()
+    assert r["loss"] == pytest.approx(math.log(7), abs=1e-14)
+    expect = np.zeros_like(H)
+    for i in np.nonzero(valid)[0]:
+        expect[i] = (W.mean(0) - W[t[i]]) / nv
+    np.testing.assert_allclose(r["dH"], expect, atol=1e-14)
+    np.testing.assert_array_equal(r["dW"], 0.0)
+
+
+def test_single_class_gives_zero():
+    H, W, _ = _rand(9, 3, 1, seed=3)
+    t = np.array([0, 0, IGNORE_INDEX, 0, 0, 0, IGNORE_INDEX, 0, 0])
+    r = oracle.forward_backward(H, W, t)
+    assert r["loss"] == 0.0
+    np.testing.assert_array_equal(r["dH"], 0.0)
+    np.testing.assert_array_equal(r["dW"], 0.0)
+
+
+def test_two_class_softplus_closed_form():
+    # d = 1, V = 2: loss_i = softplus(s_other - s_target), a logistic loss
+    g = np.random.default_rng(4)
+    N = 13
+    H = g.standard_normal((N, 1))
+    W = np.array([[0.7], [-1.3]])
+    t = g.integers(0, 2, N)
+    t[[2, 5]] = IGNORE_INDEX
+    r = oracle.forward_backward(H, W, t)
+    valid = np.nonzero(t != IGNORE_INDEX)[0]
+    nv = len(valid)
+    loss = 0.0
+    dH = np.zeros((N, 1))
+    dW = np.zeros((2, 1))
+    for i in valid:
+        h = H[i, 0]
+        o = 1 - t[i]
+        delta = h * (W[o, 0] - W[t[i], 0])
+        loss += math.log1p(math.exp(delta))
+        sig = 1.0 / (1.0 + math.exp(-delta))          # d softplus / d delta
+        dH[i, 0] = sig * (W[o, 0] - W[t[i], 0]) / nv
+        dW[o, 0] += sig * h / nv
+        dW[t[i], 0] -= sig * h / nv
+    assert r["loss"] == pytest.approx(loss / nv, rel=1e-14)
+    np.testing.assert_allclose(r["dH"], dH, rtol=1e-13, atol=1e-16)
+    np.testing.assert_allclose(r["dW"], dW, rtol=1e-13, atol=1e-16)
+
+
+def test_hand_derived_worked_example():
+    with open(os.path.join(GOLDEN, "worked_example_3x3.json")) as f:
+        ex = json.load(f)
+    ln2, ln3 = math.log(2), math.log(3)
+    H = np.array(ex["H"], dtype=float)
+    W = np.array([[0, 0], [ln2, 0], [0, ln3]])
+    t = np.array(ex["targets"])
+    r = oracle.forward_backward(H, W, t, ex["ignore_index"])
+    assert r["loss"] == pytest.approx(math.log(20) / 3, rel=1e-15)
+    np.testing.assert_allclose(np.exp(r["lse"]), [4, 5, 6], rtol=1e-15)
+    dH = np.array([[-ln2 / 2, ln3 / 4], [ln2 / 5, 3 * ln3 / 5], [ln2 / 3, -ln3 / 2], [0, 0]]) / 3
+    np.testing.assert_allclose(r["dH"], dH, rtol=1e-14, atol=1e-16)
+    dW = np.array([[1 / 4 + 1 / 6, -4 / 5 + 1 / 6],
+                   [-1 / 2 + 1 / 3, 1 / 5 + 1 / 3],
+                   [1 / 4 - 1 / 2, 3 / 5 - 1 / 2]]) / 3
+    np.testing.assert_allclose(r["dW"], dW, rtol=1e-14, atol=1e-16)
+    assert np.all(r["dH"][3] == 0.0)
+
+
+def test_no_valid_rows_gives_nan_loss_and_zero_grads():
+    H, W, _ = _rand(6, 3, 4, seed=5)
+    t = np.full(6, IGNORE_INDEX)
+    r = oracle.forward_backward(H, W, t)
+    assert math.isnan(r["loss"])
+    np.testing.assert_array_equal(r["dH"], 0.0)
+    np.testing.assert_array_equal(r["dW"], 0.0)
+    assert r["n_valid"] == 0
+
+
+# ---------------------------------------------------------- finite differences
+
+def _loss_only(H, W, t):
+    return oracle.forward(H, W, t)["loss"]
+
+
+def test_central_finite_differences():
+    H, W, t = _rand(4, 3, 5, seed=6, pad=0.0)
+    t[1] = IGNORE_INDEX
+    r = oracle.forward_backward(H, W, t)
+    eps = 1e-6
+    for A, grad in ((H, r["dH"]), (W, r["dW"])):
+        num = np.zeros_like(A)
+        for idx in np.ndindex(A.shape):
+            old = A[idx]
+            A[idx] = old + eps
+            lp = _loss_only(H, W, t)
+            A[idx] = old - eps
+            lm = _loss_only(H, W, t)
+            A[idx] = old
+            num[idx] = (lp - lm) / (2 * eps)
+        np.testing.assert_allclose(grad, num, atol=2e-9)
+
+
+# --------------------------------------------------- independent library check
+
+@pytest.mark.parametrize("shape", [(1, 1, 2), (7, 3, 5), (64, 16, 33), (200, 24, 300)])
+def test_torch_float64_autograd(shape):
+    torch = pytest.importorskip("torch")
+    N, d, V = shape
+    H, W, t = _rand(N, d, V, seed=N + d + V, scale=2.0)
+    if N > 1:
+        t[0] = IGNORE_INDEX
+    r = oracle.forward_backward(H, W, t)
+    Ht = torch.tensor(H, requires_grad=True)
+    Wt = torch.tensor(W, requires_grad=True)
+    loss = torch.nn.functional.cross_entropy(Ht @ Wt.T, torch.tensor(t), ignore_index=IGNORE_INDEX)
+    loss.backward()
+    assert r["loss"] == pytest.approx(loss.item(), rel=1e-12)
+    np.testing.assert_allclose(r["dH"], Ht.grad.numpy(), rtol=1e-10, atol=1e-15)
+    np.testing.assert_allclose(r["dW"], Wt.grad.numpy(), rtol=1e-10, atol=1e-15)
+
+
+def test_torch_float64_autograd_tiny_workload():
+    torch = pytest.importorskip("torch")
+    from synth_inputs import make_inputs
+    x = make_inputs("tiny")
+    H, W = x.H.astype(np.float64), x.W.astype(np.float64)
+    r = oracle.forward_backward(H, W, x.targets)
+    Ht = torch.tensor(H, requires_grad=True)
+    Wt = torch.tensor(W, requires_grad=True)
+    loss = torch.nn.functional.cross_entropy(Ht @ Wt.T, torch.tensor(x.targets), ignore_index=IGNORE_INDEX)
+    loss.backward()
+    assert r["n_valid"] == 230
+    assert r["loss"] == pytest.approx(loss.item(), rel=1e-12)
+    np.testing.assert_allclose(r["dH"], Ht.grad.numpy(), rtol=1e-9, atol=1e-15)
+    np.testing.assert_allclose(r["dW"], Wt.grad.numpy(), rtol=1e-9, atol=1e-15)
+
+
+# ------------------------------------------------------------------ invariants
+
+def test_columns_of_dW_sum_to_zero():
+    H, W, t = _rand(50, 6, 17, seed=7, scale=3.0)
+    r = oracle.forward_backward(H, W, t)
+    np.testing.assert_allclose(r["dW"].sum(0), 0.0, atol=1e-15)
+
+
+def test_common_shift_of_vocab_rows_changes_nothing():
+    H, W, t = _rand(40, 5, 9, seed=8)
+    c = np.random.default_rng(9).standard_normal(5)
+    a = oracle.forward_backward(H, W, t)
+    b = oracle.forward_backward(H, W + c[None, :], t)
+    assert a["loss"] == pytest.approx(b["loss"], rel=1e-12)
+    np.testing.assert_allclose(a["dH"], b["dH"], atol=1e-14)
+    np.testing.assert_allclose(a["dW"], b["dW"], atol=1e-14)
+
+
+def test_token_permutation():
+    H, W, t = _rand(31, 4, 10, seed=10)
+    p = np.random.default_rng(11).permutation(31)
+    a = oracle.forward_backward(H, W, t)
+    b = oracle.forward_backward(H[p], W, t[p])
+    assert a["loss"] == pytest.approx(b["loss"], rel=1e-13)
+    np.testing.assert_allclose(a["dH"][p], b["dH"], atol=1e-15)
+    np.testing.assert_allclose(a["dW"], b["dW"], atol=1e-15)
+
+
+def test_padded_rows_are_exact_zero_and_removable():
+    H, W, t = _rand(30, 4, 8, seed=12, pad=0.4)
+    a = oracle.forward_backward(H, W, t)
+    pad = t == IGNORE_INDEX
+    assert pad.any()
+    assert np.all(a["dH"][pad] == 0.0)
+    b = oracle.forward_backward(H[~pad], W, t[~pad])
+    assert a["loss"] == pytest.approx(b["loss"], rel=1e-14)
+    np.testing.assert_allclose(a["dH"][~pad], b["dH"], atol=1e-16)
+    np.testing.assert_allclose(a["dW"], b["dW"], atol=1e-16)
+    # padded rows' H values must not matter at all
+    H2 = H.copy()
+    H2[pad] = 1e6
+    c = oracle.forward_backward(H2, W, t)
+    np.testing.assert_array_equal(a["dW"], c["dW"])
+
+
+def test_normaliser_is_valid_count_not_N():
+    H, W, t = _rand(20, 3, 6, seed=13, pad=0.0)
+    t[:10] = IGNORE_INDEX
+    r = oracle.forward_backward(H, W, t)
+    assert r["loss"] == pytest.approx(r["loss_rows"].mean(), rel=1e-14)
+    assert r["n_valid"] == 10
+
+
+# --------------------------------------------------------------- compaction
+
+def test_compaction_golden_cases():
+    with open(os.path.join(GOLDEN, "compaction_small.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        t = np.array(c["targets"], dtype=np.int64)
+        assert oracle.valid_rows(t, c["ignore_index"]).tolist() == c["valid"]
+        assert oracle.out_of_range_targets(t, c["ignore_index"], c["V"]) == c["out_of_range"]
+
+
+def test_compaction_brute_force():
+    g = np.random.default_rng(14)
+    for n in (0, 1, 31, 32, 33, 1000, 4097):
+        t = g.integers(-3, 5, n)
+        t[g.random(n) < 0.3] = IGNORE_INDEX
+        expect = [i for i in range(n) if t[i] != IGNORE_INDEX]
+        assert oracle.valid_rows(t, IGNORE_INDEX).tolist() == expect
+
+
+def test_out_of_range_target_is_refused():
+    H, W, t = _rand(5, 2, 3, seed=15, pad=0.0)
+    t[2] = 3
+    with pytest.raises(ValueError):
+        oracle.forward_backward(H, W, t)
+
+
+# ------------------------------------------------------- sampled reference
+
+def test_sampled_reference_matches_full():
+    H, W, t = _rand(300, 8, 70, seed=16, scale=2.0)
+    full = oracle.forward_backward(H, W, t)
+    rows = np.array([0, 5, 17, 299, 123])
+    vocab = np.array([0, 69, 33, 1])
+    s = oracle.sampled_reference(H, W, t, IGNORE_INDEX, rows, vocab)
+    assert s["loss"] == pytest.approx(full["loss"], rel=1e-13)
+    np.testing.assert_allclose(s["dH_rows"], full["dH"][rows], atol=1e-15)
+    np.testing.assert_allclose(s["dW_rows"], full["dW"][vocab], atol=1e-15)
