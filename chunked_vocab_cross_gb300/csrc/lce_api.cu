@@ -1,0 +1,523 @@
+// Host runtime and C ABI of liblce: argument checks, workspace layout, TMA
+// tensor-map encoding, and the launch sequence of the fused output-projection
+// + cross-entropy path on the caller's stream.
+//
+// Sequence (all on `stream`, no host synchronisation):
+//   1 k_compact        valid rows -> idx / inv / Nv (device)
+//   2 k_gather         Hc = H[idx], zero-padded to 128-row blocks
+//   3 k_gemm<LSE>      logits tiles + online log-sum-exp partials + target logit
+//   4 k_lse_merge      lse per row, loss_i
+//   5 k_loss_reduce    loss = mean loss_i
+//   backward, per vocab chunk c of Vc rows:
+//   6 k_gemm<G>        recompute logits of the chunk, G = (softmax - onehot)/Nv
+//   7 k_gemm<DW>       dW[chunk] = G^T Hc
+//   8 k_gemm<DH>       dHacc (+)= G W[chunk]
+//   9 k_dh_scatter     dH = dHacc[inv], zero on ignored rows
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "lce.h"
+#include "lce_gemm.cuh"
+#include "lce_rows.cuh"
+
+using namespace lce;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxSms = 256;              // bound used to size the (m, l) partials
+constexpr int64_t kDefaultVocabChunk = 4096;
+
+thread_local int t_last_cuda = 0;
+std::atomic<int64_t> g_launches{0};
+std::mutex g_mu;
+
+struct DevInfo {
+    bool ready = false;
+    int sms = 0, major = 0, minor = 0;
+};
+DevInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// ----------------------------------------------------------------- profiling
+
+struct PhaseRec {
+    int phase;
+    cudaEvent_t a, b;
+    int64_t launches;
+};
+struct Profiler {
+    bool on = false;
+    std::vector<PhaseRec> recs;
+    int64_t *cur = nullptr;
+};
+thread_local Profiler t_prof;
+
+struct PhaseScope {
+    cudaStream_t s;
+    PhaseRec rec{};
+    bool live = false;
+    int64_t launches = 0;
+    PhaseScope(int phase, cudaStream_t st) : s(st) {
+        if (!t_prof.on) return;
+        rec.phase = phase;
+        if (cudaEventCreate(&rec.a) != cudaSuccess) return;
+        if (cudaEventCreate(&rec.b) != cudaSuccess) {
+            cudaEventDestroy(rec.a);
+            return;
+        }
+        cudaEventRecord(rec.a, s);
+        live = true;
+        t_prof.cur = &launches;
+    }
+    ~PhaseScope() {
+        if (!live) return;
+        cudaEventRecord(rec.b, s);
+        rec.launches = launches;
+        t_prof.recs.push_back(rec);
+        t_prof.cur = nullptr;
+    }
+};
+
+inline void count_launch() {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (t_prof.cur) ++*t_prof.cur;
+}
+
+// -------------------------------------------------------------------- device
+
+lce_status_t device_info(DevInfo **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        t_last_cuda = e;
+        return LCE_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return LCE_ERR_DEVICE;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevInfo &di = g_dev[dev];
+    if (!di.ready) {
+        cudaDeviceProp p;
+        e = cudaGetDeviceProperties(&p, dev);
+        if (e != cudaSuccess) {
+            t_last_cuda = e;
+            return LCE_ERR_CUDA;
+        }
+        di.sms = p.multiProcessorCount;
+        di.major = p.major;
+        di.minor = p.minor;
+        if (!(di.major == 10 && di.minor == 3) || di.sms > kMaxSms) return LCE_ERR_DEVICE;
+        const void *gemms[] = {
+            (const void *)k_gemm<__nv_bfloat16, MODE_LSE>, (const void *)k_gemm<__nv_bfloat16, MODE_G>,
+            (const void *)k_gemm<__nv_bfloat16, MODE_DH>,  (const void *)k_gemm<__nv_bfloat16, MODE_DW>,
+            (const void *)k_gemm<float, MODE_LSE>,         (const void *)k_gemm<float, MODE_G>,
+            (const void *)k_gemm<float, MODE_DH>,          (const void *)k_gemm<float, MODE_DW>,
+        };
+        for (const void *f : gemms) {
+            e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+            if (e != cudaSuccess) {
+                t_last_cuda = e;
+                return LCE_ERR_CUDA;
+            }
+        }
+        if (!g_encode) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+                t_last_cuda = e != cudaSuccess ? e : cudaErrorNotSupported;
+                return LCE_ERR_CUDA;
+            }
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        di.ready = true;
+    }
+    *out = &di;
+    return LCE_OK;
+}
+
+bool encode_map(CUtensorMap *m, lce_dtype_t dt, const void *base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                uint32_t box_outer) {
+    const uint64_t elt = dt == LCE_BF16 ? 2 : 4;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * elt};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = g_encode(m, dt == LCE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                          const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// ----------------------------------------------------------------- workspace
+
+inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Layout {
+    int64_t N_pad = 0, Vc = 0, part_rows = 0;
+    size_t idx = 0, inv = 0, counters = 0, tc = 0, z = 0, lse2 = 0, loss_rows = 0, part = 0, Hc = 0, G = 0,
+           dHacc = 0, total = 0;
+};
+
+Layout make_layout(int64_t N, int64_t d, int64_t V, lce_dtype_t dt, int64_t Vc, bool backward) {
+    Layout L;
+    const size_t elt = dt == LCE_BF16 ? 2 : 4;
+    L.N_pad = (N + kBM - 1) / kBM * kBM;
+    L.Vc = Vc;
+    L.part_rows = lse_partial_rows(static_cast<int>(L.N_pad), kMaxSms);
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o += up256(bytes);
+        return at;
+    };
+    L.idx = take(N * 4);
+    L.inv = take(N * 4);
+    L.counters = take(64);
+    L.tc = take(L.N_pad * 4);
+    L.z = take(L.N_pad * 4);
+    L.lse2 = take(L.N_pad * 4);
+    L.loss_rows = take(L.N_pad * 4);
+    L.part = take(L.part_rows * 8);
+    L.Hc = take(L.N_pad * d * elt);
+    if (backward) {
+        L.G = take(L.N_pad * Vc * elt);
+        L.dHacc = take(L.N_pad * d * 4);
+    }
+    L.total = o;
+    return L;
+}
+
+int64_t pick_chunk(int64_t V, int64_t requested) {
+    const int64_t vpad = (V + kBN - 1) / kBN * kBN;
+    int64_t c = requested > 0 ? requested : kDefaultVocabChunk;
+    return c < vpad ? c : vpad;
+}
+
+lce_status_t check_args(const lce_args_t *a) {
+    if (!a) return LCE_ERR_NULL;
+    if (a->dtype != LCE_BF16 && a->dtype != LCE_FP32) return LCE_ERR_DTYPE;
+    if (!a->H || !a->W || !a->targets || !a->loss) return LCE_ERR_NULL;
+    if ((a->dH == nullptr) != (a->dW == nullptr)) return LCE_ERR_NULL;
+    if (a->N < 1 || a->N >= (int64_t(1) << 31) || a->d < 1 || a->d > 65536 || a->V < 1 ||
+        a->V >= (int64_t(1) << 31))
+        return LCE_ERR_SHAPE;
+    if (a->vocab_chunk < 0 || (a->vocab_chunk > 0 && (a->vocab_chunk % kBN) != 0) ||
+        a->vocab_chunk > (int64_t(1) << 20))
+        return LCE_ERR_SHAPE;
+    const int64_t elt = a->dtype == LCE_BF16 ? 2 : 4;
+    if ((a->d * elt) % 16) return LCE_ERR_ALIGN;
+    auto mis = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+    if (mis(a->H) || mis(a->W) || (a->dH && mis(a->dH)) || (a->dW && mis(a->dW)) ||
+        (a->workspace && mis(a->workspace)))
+        return LCE_ERR_ALIGN;
+    return LCE_OK;
+}
+
+struct WsGuard {
+    void *p = nullptr;
+    cudaStream_t s = nullptr;
+    bool owned = false;
+    ~WsGuard() {
+        if (owned && p) cudaFreeAsync(p, s);
+    }
+};
+
+#define LCE_CHECK_LAUNCH()                     \
+    do {                                       \
+        count_launch();                        \
+        cudaError_t e_ = cudaGetLastError();   \
+        if (e_ != cudaSuccess) {               \
+            t_last_cuda = e_;                  \
+            return LCE_ERR_CUDA;               \
+        }                                      \
+    } while (0)
+
+template <typename T>
+lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(a->stream);
+    const bool backward = a->dH != nullptr;
+    const int64_t Vc = pick_chunk(a->V, a->vocab_chunk);
+    const Layout L = make_layout(a->N, a->d, a->V, a->dtype, Vc, backward);
+    const int N = static_cast<int>(a->N), d = static_cast<int>(a->d), V = static_cast<int>(a->V);
+
+    WsGuard ws;
+    ws.s = st;
+    if (a->workspace) {
+        if (a->workspace_bytes < L.total) return LCE_ERR_WORKSPACE;
+        ws.p = a->workspace;
+    } else {
+        cudaError_t e = cudaMallocAsync(&ws.p, L.total, st);
+        if (e != cudaSuccess) {
+            t_last_cuda = e;
+            return LCE_ERR_CUDA;
+        }
+        ws.owned = true;
+    }
+    uint8_t *base = static_cast<uint8_t *>(ws.p);
+    int *idx = reinterpret_cast<int *>(base + L.idx);
+    int *inv = reinterpret_cast<int *>(base + L.inv);
+    int *counters = reinterpret_cast<int *>(base + L.counters);
+    int *tc = reinterpret_cast<int *>(base + L.tc);
+    float *z = reinterpret_cast<float *>(base + L.z);
+    float *lse2 = reinterpret_cast<float *>(base + L.lse2);
+    float *loss_rows = reinterpret_cast<float *>(base + L.loss_rows);
+    float2 *part = reinterpret_cast<float2 *>(base + L.part);
+    T *Hc = reinterpret_cast<T *>(base + L.Hc);
+    T *G = backward ? reinterpret_cast<T *>(base + L.G) : nullptr;
+    float *dHacc = backward ? reinterpret_cast<float *>(base + L.dHacc) : nullptr;
+
+    const int bk = Tile<T>::kBK;
+    const int atom = Tile<T>::kAtom;
+    CUtensorMap tmHc_k, tmW_k;
+    if (!encode_map(&tmHc_k, a->dtype, Hc, d, L.N_pad, bk, kBM) ||
+        !encode_map(&tmW_k, a->dtype, a->W, d, V, bk, kBN))
+        return LCE_ERR_CUDA;
+
+    GemmArgs ga{};
+    ga.counters = counters;
+    ga.d = d;
+    ga.V = V;
+    ga.num_sms = di.sms;
+    ga.tc = tc;
+    ga.grad_scale = a->grad_scale == 0.f ? 1.f : a->grad_scale;
+    const int n_tiles_v = cdiv(V, kBN);
+
+    {
+        PhaseScope ph(0, st);
+        k_compact<<<1, kCompactThreads, 0, st>>>(a->targets, N, a->ignore_index, a->V, idx, inv, counters, a->lse);
+        LCE_CHECK_LAUNCH();
+        const int grid = static_cast<int>(L.N_pad < 4 * di.sms * 8 ? L.N_pad : 4 * di.sms * 8);
+        k_gather<T><<<grid, 256, 0, st>>>(static_cast<const T *>(a->H), a->targets, d, a->V, idx, counters, Hc, tc,
+                                           z);
+        LCE_CHECK_LAUNCH();
+    }
+    {
+        PhaseScope ph(1, st);
+        GemmArgs g = ga;
+        g.v0 = 0;
+        g.vlen = V;
+        g.z = z;
+        g.part = part;
+        k_gemm<T, MODE_LSE><<<di.sms, kThreads, kGemmSmem, st>>>(tmHc_k, tmW_k, g);
+        LCE_CHECK_LAUNCH();
+    }
+    {
+        PhaseScope ph(2, st);
+        k_lse_merge<<<static_cast<int>(L.N_pad / 256 + 1), 256, 0, st>>>(part, counters, n_tiles_v, di.sms, z, lse2,
+                                                                         loss_rows, idx, a->lse);
+        LCE_CHECK_LAUNCH();
+        k_loss_reduce<<<1, 1024, 0, st>>>(loss_rows, counters, a->loss);
+        LCE_CHECK_LAUNCH();
+    }
+    if (!backward) return LCE_OK;
+
+    CUtensorMap tmG_k, tmG_mn, tmHc_mn, tmW_mn;
+    if (!encode_map(&tmG_k, a->dtype, G, Vc, L.N_pad, bk, kBM) ||
+        !encode_map(&tmG_mn, a->dtype, G, Vc, L.N_pad, atom, bk) ||
+        !encode_map(&tmHc_mn, a->dtype, Hc, d, L.N_pad, atom, bk) ||
+        !encode_map(&tmW_mn, a->dtype, a->W, d, V, atom, bk))
+        return LCE_ERR_CUDA;
+
+    const int dw_grid_cap = di.sms;
+    for (int64_t v0 = 0; v0 < a->V; v0 += Vc) {
+        const int vlen = static_cast<int>(a->V - v0 < Vc ? a->V - v0 : Vc);
+        GemmArgs g = ga;
+        g.v0 = static_cast<int>(v0);
+        g.vlen = vlen;
+        g.ldg = static_cast<int>(Vc);
+        g.G = G;
+        g.lse2 = lse2;
+        {
+            PhaseScope ph(3, st);
+            k_gemm<T, MODE_G><<<di.sms, kThreads, kGemmSmem, st>>>(tmHc_k, tmW_k, g);
+            LCE_CHECK_LAUNCH();
+        }
+        {
+            PhaseScope ph(4, st);
+            GemmArgs gw = g;
+            gw.dW = a->dW;
+            gw.accumulate = a->accumulate_dW ? 1 : 0;
+            const int units = cdiv(vlen, kBM) * cdiv(d, kBN);
+            k_gemm<T, MODE_DW><<<units < dw_grid_cap ? units : dw_grid_cap, kThreads, kGemmSmem, st>>>(tmG_mn,
+                                                                                                      tmHc_mn, gw);
+            LCE_CHECK_LAUNCH();
+        }
+        {
+            PhaseScope ph(5, st);
+            GemmArgs gh = g;
+            gh.dH_acc = dHacc;
+            gh.accumulate = v0 > 0 ? 1 : 0;
+            k_gemm<T, MODE_DH><<<di.sms, kThreads, kGemmSmem, st>>>(tmG_k, tmW_mn, gh);
+            LCE_CHECK_LAUNCH();
+        }
+    }
+    {
+        PhaseScope ph(5, st);
+        const int grid = N < 8 * di.sms ? N : 8 * di.sms;
+        k_dh_scatter<T><<<grid, 256, 0, st>>>(dHacc, inv, N, d, static_cast<T *>(a->dH));
+        LCE_CHECK_LAUNCH();
+    }
+    return LCE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+lce_status_t lce_run(const lce_args_t *a) {
+    lce_status_t s = check_args(a);
+    if (s != LCE_OK) return s;
+    DevInfo *di = nullptr;
+    s = device_info(&di);
+    if (s != LCE_OK) return s;
+    return a->dtype == LCE_BF16 ? run_typed<__nv_bfloat16>(a, *di) : run_typed<float>(a, *di);
+}
+
+lce_status_t lce_forward(const void *H, const void *W, const int64_t *targets, int64_t ignore_index, int64_t N,
+                         int64_t d, int64_t V, float *loss, lce_stream_t stream) {
+    lce_args_t a{};
+    a.dtype = LCE_BF16;
+    a.H = H;
+    a.W = W;
+    a.targets = targets;
+    a.ignore_index = ignore_index;
+    a.N = N;
+    a.d = d;
+    a.V = V;
+    a.loss = loss;
+    a.stream = stream;
+    return lce_run(&a);
+}
+
+lce_status_t lce_forward_backward(const void *H, const void *W, const int64_t *targets, int64_t ignore_index,
+                                  int64_t N, int64_t d, int64_t V, float *loss, void *dH, float *dW,
+                                  lce_stream_t stream) {
+    if (!dH || !dW) return LCE_ERR_NULL;
+    lce_args_t a{};
+    a.dtype = LCE_BF16;
+    a.H = H;
+    a.W = W;
+    a.targets = targets;
+    a.ignore_index = ignore_index;
+    a.N = N;
+    a.d = d;
+    a.V = V;
+    a.loss = loss;
+    a.dH = dH;
+    a.dW = dW;
+    a.stream = stream;
+    return lce_run(&a);
+}
+
+lce_status_t lce_compact(const int64_t *targets, int64_t N, int64_t ignore_index, int64_t V, int32_t *idx,
+                         int32_t *inv, int32_t *counts, lce_stream_t stream) {
+    if (!targets || !idx || !inv || !counts) return LCE_ERR_NULL;
+    if (N < 1 || N >= (int64_t(1) << 31) || V < 1 || V >= (int64_t(1) << 31)) return LCE_ERR_SHAPE;
+    DevInfo *di = nullptr;
+    lce_status_t s = device_info(&di);
+    if (s != LCE_OK) return s;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    PhaseScope ph(0, st);
+    k_compact<<<1, kCompactThreads, 0, st>>>(targets, static_cast<int>(N), ignore_index, V, idx, inv, counts,
+                                             nullptr);
+    LCE_CHECK_LAUNCH();
+    return LCE_OK;
+}
+
+size_t lce_workspace_size(int64_t N, int64_t d, int64_t V, lce_dtype_t dtype, int64_t vocab_chunk) {
+    if (N < 1 || N >= (int64_t(1) << 31) || d < 1 || d > 65536 || V < 1 || V >= (int64_t(1) << 31)) return 0;
+    if (dtype != LCE_BF16 && dtype != LCE_FP32) return 0;
+    if (vocab_chunk < 0 || (vocab_chunk > 0 && vocab_chunk % kBN)) return 0;
+    return make_layout(N, d, V, dtype, pick_chunk(V, vocab_chunk), true).total;
+}
+
+lce_status_t lce_get_device_status(lce_stream_t stream, int32_t *bits) {
+    if (!bits) return LCE_ERR_NULL;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        t_last_cuda = e;
+        return LCE_ERR_CUDA;
+    }
+    int v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_status, sizeof(int));
+    if (e != cudaSuccess) {
+        t_last_cuda = e;
+        return LCE_ERR_CUDA;
+    }
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_status, &zero, sizeof(int));
+    if (e != cudaSuccess) {
+        t_last_cuda = e;
+        return LCE_ERR_CUDA;
+    }
+    *bits = v;
+    if (v & LCE_DEV_TARGET_RANGE) return LCE_ERR_TARGET_RANGE;
+    if (v & LCE_DEV_TIMEOUT) return LCE_ERR_TIMEOUT;
+    return LCE_OK;
+}
+
+const char *lce_status_string(lce_status_t s) {
+    switch (s) {
+        case LCE_OK: return "ok";
+        case LCE_ERR_NULL: return "a required pointer is NULL";
+        case LCE_ERR_SHAPE: return "N, d, V or vocab_chunk out of range";
+        case LCE_ERR_ALIGN: return "pointer or row stride not 16-byte aligned";
+        case LCE_ERR_DTYPE: return "unknown dtype";
+        case LCE_ERR_CUDA: return "a CUDA call failed";
+        case LCE_ERR_WORKSPACE: return "workspace smaller than lce_workspace_size()";
+        case LCE_ERR_TARGET_RANGE: return "a non-ignored target is outside [0, V)";
+        case LCE_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up";
+        case LCE_ERR_DEVICE: return "the current device is not sm_103";
+    }
+    return "unknown status";
+}
+
+int lce_last_cuda_error(void) { return t_last_cuda; }
+
+int64_t lce_launch_count(void) { return g_launches.load(); }
+
+lce_status_t lce_profile_begin(void) {
+    for (auto &r : t_prof.recs) {
+        cudaEventDestroy(r.a);
+        cudaEventDestroy(r.b);
+    }
+    t_prof.recs.clear();
+    t_prof.on = true;
+    return LCE_OK;
+}
+
+lce_status_t lce_profile_end(double *ms, int64_t *launches, int n) {
+    t_prof.on = false;
+    lce_status_t st = LCE_OK;
+    for (int i = 0; i < n; ++i) {
+        if (ms) ms[i] = 0.0;
+        if (launches) launches[i] = 0;
+    }
+    for (auto &r : t_prof.recs) {
+        float t = 0.f;
+        cudaError_t e = cudaEventSynchronize(r.b);
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&t, r.a, r.b);
+        if (e != cudaSuccess) {
+            t_last_cuda = e;
+            st = LCE_ERR_CUDA;
+        } else if (r.phase < n) {
+            if (ms) ms[r.phase] += t;
+            if (launches) launches[r.phase] += r.launches;
+        }
+        cudaEventDestroy(r.a);
+        cudaEventDestroy(r.b);
+    }
+    t_prof.recs.clear();
+    return st;
+}
+
+int lce_version(void) { return 100; }
+
+}  // extern "C"

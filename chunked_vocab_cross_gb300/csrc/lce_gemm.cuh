@@ -1,0 +1,480 @@
+// Persistent, warp-specialised tcgen05 GEMM engine with the four fused
+// epilogues of the output-projection + cross-entropy path.
+//
+// One CTA per SM, 192 threads:
+//   warp 0      TMA producer: streams A and B k-blocks into a 4-stage
+//               shared-memory ring (128-byte swizzle), signalling mbarriers.
+//   warp 1      owns TMEM (512 columns = two 128x256 fp32 accumulators) and
+//               issues tcgen05.mma 128x256xK from one thread.
+//   warps 2..5  epilogue: tcgen05.ld the finished accumulator (warp w reads
+//               TMEM lanes 32*(w%4)..+31, one tile row per thread) while the
+//               MMA thread already fills the other accumulator.
+//
+// Modes (A x B^T, all operands bf16 or tf32 in shared memory, fp32 in TMEM):
+//   MODE_LSE  S = Hc . W^T      per 128-row block over a contiguous range of
+//             256-wide vocab tiles; the epilogue carries the online
+//             (max, sum) of exp over the row in registers and writes one
+//             (m, l) partial per row and range, plus the target logit.
+//   MODE_G    S = Hc . W_c^T    over one vocab chunk; the epilogue forms
+//             G = (exp(S - lse) - onehot) * scale / Nv and stores it.
+//   MODE_DW   dW_c = G^T . Hc   (M = chunk vocab rows, K = valid tokens);
+//             A and B are read MN-major straight from G and Hc.
+//   MODE_DH   dHacc += G . W_c  (M = valid tokens, K = chunk vocab rows);
+//             B is read MN-major straight from W.
+//
+// Every wait is bounded: on time-out the CTA raises LCE_DEV_TIMEOUT in the
+// device status word, lets its in-flight copies and MMAs land, frees TMEM and
+// returns.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "tc_ptx.cuh"
+
+namespace lce {
+
+constexpr int kBM = 128;          // tile rows   (UMMA M)
+constexpr int kBN = 256;          // tile cols   (UMMA N)
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;    // two 256-column fp32 accumulators
+constexpr int kStageA = kBM * 128;
+constexpr int kStageB = kBN * 128;
+constexpr int kStageBytes = kStageA + kStageB;
+constexpr int kGemmSmem = kStages * kStageBytes + 1024 /*alignment slack*/ + 256 /*barriers*/;
+constexpr long long kWaitCycles = 2000000000LL;   // ~1 s: far above any legitimate wait
+constexpr long long kDrainCycles = 200000000LL;
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum GemmMode : int { MODE_LSE = 0, MODE_G = 1, MODE_DH = 2, MODE_DW = 3 };
+enum DevStatus : int { DEV_TARGET_RANGE = 1, DEV_TIMEOUT = 2 };
+
+// Device status word (LCE_DEV_* bits). The library is one translation unit,
+// so this header is the single definition.
+__device__ int g_status = 0;
+
+template <typename T>
+struct Elem;
+template <>
+struct Elem<__nv_bfloat16> {
+    static constexpr uint32_t kFmt = 1;   // bf16
+};
+template <>
+struct Elem<float> {
+    static constexpr uint32_t kFmt = 2;   // tf32
+};
+
+template <typename T>
+struct Tile {
+    static constexpr int kBytes = sizeof(T);
+    static constexpr int kBK = 128 / kBytes;        // k per stage: one 128-byte line
+    static constexpr int kUmmaK = 32 / kBytes;      // k per tcgen05.mma
+    static constexpr int kAtom = 128 / kBytes;      // MN elements per 128-byte line
+    static constexpr int kAtomBytes = kBK * 128;    // one MN-major box {kAtom, kBK}
+};
+
+__host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// Vocab splits for MODE_LSE: choose the number of contiguous vocab ranges per
+// row block so that m_blocks*splits units fill whole waves of `sms` CTAs with
+// the shortest longest-CTA time, ceil(units/sms) * ceil(n_tiles/splits).
+__host__ __device__ inline int lse_splits(int m_blocks, int n_tiles, int sms) {
+    if (m_blocks <= 0 || n_tiles <= 1) return 1;
+    int best = 1;
+    long long best_cost = static_cast<long long>(cdiv(m_blocks, sms)) * n_tiles;
+    for (int w = 1; w <= 16; ++w) {
+        int s = (w * sms) / m_blocks;
+        if (s < 1) continue;
+        if (s > n_tiles) s = n_tiles;
+        long long cost = static_cast<long long>(cdiv(m_blocks * s, sms)) * cdiv(n_tiles, s);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
+}
+
+// Largest number of (m, l) partial rows MODE_LSE can write for row capacity
+// `rows_cap` (a multiple of 128).
+__host__ __device__ inline long long lse_partial_rows(int rows_cap, int sms) {
+    long long a = 16LL * sms, b = rows_cap / kBM;
+    return (a > b ? a : b) * kBM;
+}
+
+struct GemmArgs {
+    const int *counters;   // counters[0] = Nv (written by the compaction kernel)
+    int d, V;
+    int v0;                // first vocab row of the chunk (0 for MODE_LSE)
+    int vlen;              // vocab rows in the chunk (V for MODE_LSE)
+    int num_sms;
+    int ldg;               // row stride of G in elements
+    const int *tc;         // compacted targets, -1 where none
+    const float *lse2;     // per compacted row: lse / ln 2   (MODE_G)
+    float *z;              // per compacted row: target logit (MODE_LSE)
+    float2 *part;          // (m, l) partials [splits][m_blocks*128] (MODE_LSE)
+    void *G;               // G chunk [rows][ldg]            (MODE_G)
+    float *dW;             // [V][d]                           (MODE_DW)
+    float *dH_acc;         // [rows][d]                        (MODE_DH)
+    int accumulate;        // DW / DH: add into the output instead of overwriting
+    float grad_scale;      // MODE_G: multiplies G
+};
+
+struct Sched {
+    int m_blocks, n_tiles, k_blocks, splits, units;
+};
+
+template <typename T, int MODE>
+__device__ inline Sched make_sched(const GemmArgs &a, int nv) {
+    Sched s;
+    const int bk = Tile<T>::kBK;
+    s.splits = 1;
+    if (MODE == MODE_LSE || MODE == MODE_G) {
+        s.m_blocks = cdiv(nv, kBM);
+        s.n_tiles = cdiv(a.vlen, kBN);
+        s.k_blocks = cdiv(a.d, bk);
+    } else if (MODE == MODE_DH) {
+        s.m_blocks = cdiv(nv, kBM);
+        s.n_tiles = cdiv(a.d, kBN);
+        s.k_blocks = cdiv(a.vlen, bk);
+    } else {
+        s.m_blocks = cdiv(a.vlen, kBM);
+        s.n_tiles = cdiv(a.d, kBN);
+        s.k_blocks = cdiv(nv, bk);
+    }
+    if (MODE == MODE_LSE) {
+        s.splits = lse_splits(s.m_blocks, s.n_tiles, a.num_sms);
+        s.units = s.m_blocks * s.splits;
+    } else {
+        s.units = s.m_blocks * s.n_tiles;
+    }
+    return s;
+}
+
+// Unit u -> row block and [n_begin, n_end) of column tiles.
+//   LSE: split-major so CTAs running together share vocab tiles of W in L2.
+//   G, DH: column-tile-major, row blocks fastest (W / G tiles shared in L2).
+//   DW: row(vocab)-block-major, d tiles fastest (a G column block is shared).
+template <int MODE>
+__device__ inline void unit_tiles(const Sched &s, int u, int &mb, int &n0, int &n1, int &split) {
+    if (MODE == MODE_LSE) {
+        split = u / s.m_blocks;
+        mb = u % s.m_blocks;
+        n0 = static_cast<int>(static_cast<long long>(split) * s.n_tiles / s.splits);
+        n1 = static_cast<int>(static_cast<long long>(split + 1) * s.n_tiles / s.splits);
+    } else if (MODE == MODE_DW) {
+        split = 0;
+        mb = u / s.n_tiles;
+        n0 = u % s.n_tiles;
+        n1 = n0 + 1;
+    } else {
+        split = 0;
+        mb = u % s.m_blocks;
+        n0 = u / s.m_blocks;
+        n1 = n0 + 1;
+    }
+}
+
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const long long t0 = clock64();
+    for (;;) {
+        if (mbar_try_wait(a, parity)) return true;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitCycles) {
+            *abort_flag = 1;
+            atomicOr(&g_status, DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Wait used only while shutting down after an abort: ignores the abort flag.
+__device__ __forceinline__ void drain_bar(uint64_t *bar, uint32_t parity) {
+    const uint32_t a = smem_u32(bar);
+    const long long t0 = clock64();
+    while (!mbar_try_wait(a, parity)) {
+        if (clock64() - t0 > kDrainCycles) return;
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+template <typename T, int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
+    using TT = Tile<T>;
+    constexpr bool kAmn = (MODE == MODE_DW);
+    constexpr bool kBmn = (MODE == MODE_DH || MODE == MODE_DW);
+    constexpr uint32_t kIdesc = idesc_f32acc(Elem<T>::kFmt, kBM, kBN, kAmn, kBmn);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
+    uint64_t *empty = full + kStages;
+    uint64_t *tfull = empty + kStages;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *mma_done = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int nv = a.counters[0];
+    const Sched s = make_sched<T, MODE>(a, nv);
+    if (static_cast<int>(blockIdx.x) >= s.units) return;   // uniform over the CTA
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], 4);
+        }
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int it = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < s.units; u += gridDim.x) {
+                int mb, n0, n1, sp;
+                unit_tiles<MODE>(s, u, mb, n0, n1, sp);
+                for (int nt = n0; ok && nt < n1; ++nt) {
+                    for (int kb = 0; kb < s.k_blocks; ++kb, ++it) {
+                        const int st = it % kStages;
+                        if (!wait_bar(&empty[st], ((it / kStages) & 1) ^ 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&full[st], kStageBytes);
+                        uint8_t *sa = smem + st * kStageBytes;
+                        uint8_t *sb = sa + kStageA;
+                        const int k0 = kb * TT::kBK;
+                        if (MODE == MODE_LSE || MODE == MODE_G) {
+                            tma_load_2d(sa, &tmA, &full[st], k0, mb * kBM);
+                            tma_load_2d(sb, &tmB, &full[st], k0, a.v0 + nt * kBN);
+                        } else if (MODE == MODE_DH) {
+                            tma_load_2d(sa, &tmA, &full[st], k0, mb * kBM);
+#pragma unroll
+                            for (int b = 0; b < kBN / TT::kAtom; ++b)
+                                tma_load_2d(sb + b * TT::kAtomBytes, &tmB, &full[st], nt * kBN + b * TT::kAtom,
+                                            a.v0 + k0);
+                        } else {
+#pragma unroll
+                            for (int b = 0; b < kBM / TT::kAtom; ++b)
+                                tma_load_2d(sa + b * TT::kAtomBytes, &tmA, &full[st], mb * kBM + b * TT::kAtom, k0);
+#pragma unroll
+                            for (int b = 0; b < kBN / TT::kAtom; ++b)
+                                tma_load_2d(sb + b * TT::kAtomBytes, &tmB, &full[st], nt * kBN + b * TT::kAtom, k0);
+                        }
+                    }
+                }
+            }
+            if (!ok) {
+                // let the copies already issued land before the CTA exits
+                const int first = it > kStages ? it - kStages : 0;
+                for (int j = first; j < it; ++j) drain_bar(&full[j % kStages], (j / kStages) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            int it = 0, tile = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < s.units; u += gridDim.x) {
+                int mb, n0, n1, sp;
+                unit_tiles<MODE>(s, u, mb, n0, n1, sp);
+                for (int nt = n0; ok && nt < n1; ++nt, ++tile) {
+                    const int acc = tile & 1;
+                    if (!wait_bar(&tempty[acc], ((tile >> 1) & 1) ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + acc * kBN;
+                    for (int kb = 0; kb < s.k_blocks; ++kb, ++it) {
+                        const int st = it % kStages;
+                        if (!wait_bar(&full[st], (it / kStages) & 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sa = smem_u32(smem + st * kStageBytes);
+                        const uint32_t sb = sa + kStageA;
+#pragma unroll
+                        for (int kk = 0; kk < TT::kBK / TT::kUmmaK; ++kk) {
+                            const uint64_t ad = kAmn ? sdesc_sw128(sa + kk * TT::kUmmaK * 128, TT::kAtomBytes, 1024)
+                                                     : sdesc_sw128(sa + kk * 32, 16, 1024);
+                            const uint64_t bd = kBmn ? sdesc_sw128(sb + kk * TT::kUmmaK * 128, TT::kAtomBytes, 1024)
+                                                     : sdesc_sw128(sb + kk * 32, 16, 1024);
+                            if (sizeof(T) == 2)
+                                umma_f16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0);
+                            else
+                                umma_tf32(d_tmem, ad, bd, kIdesc, (kb | kk) != 0);
+                        }
+                        umma_commit(&empty[st]);   // frees the stage once these MMAs have read it
+                    }
+                    if (!ok) break;
+                    umma_commit(&tfull[acc]);      // accumulator ready for the epilogue
+                }
+            }
+            umma_commit(mma_done);
+            drain_bar(mma_done, 0);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quarter = warp & 3;
+        const int trow = quarter * 32 + lane;     // row within the tile == TMEM lane
+        const float inv_nv = nv > 0 ? a.grad_scale / static_cast<float>(nv) : 0.f;
+        int tile = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < s.units; u += gridDim.x) {
+            int mb, n0, n1, sp;
+            unit_tiles<MODE>(s, u, mb, n0, n1, sp);
+            const int grow = mb * kBM + trow;      // compacted row (LSE/G/DH) or chunk vocab row (DW)
+            int tgt = -1;
+            float lse2 = 0.f;
+            if (MODE == MODE_LSE || MODE == MODE_G) tgt = grow < nv ? a.tc[grow] : -1;
+            if (MODE == MODE_G) lse2 = grow < nv ? a.lse2[grow] : INFINITY;
+            float run_m = -INFINITY, run_l = 0.f;
+            for (int nt = n0; nt < n1; ++nt, ++tile) {
+                const int acc = tile & 1;
+                if (!wait_bar(&tfull[acc], (tile >> 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN;
+#pragma unroll 1
+                for (int c = 0; c < kBN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tbase + c * 32, r);
+                    tmem_ld_wait();
+                    const int col = nt * kBN + c * 32;   // column within the chunk / d
+                    if (MODE == MODE_LSE) {
+                        const int rel = tgt - col;
+                        if (static_cast<unsigned>(rel) < 32u) {
+                            float zv = 0.f;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (j == rel) zv = __uint_as_float(r[j]);
+                            a.z[grow] = zv;
+                        }
+                        float x[32];
+                        float cm = -INFINITY;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            x[j] = (col + j < a.vlen) ? __uint_as_float(r[j]) * kLog2e : -INFINITY;
+                            cm = fmaxf(cm, x[j]);
+                        }
+                        const float mn = fmaxf(run_m, cm);
+                        if (mn != -INFINITY) {
+                            float sum = 0.f;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) sum += exp2f(x[j] - mn);
+                            run_l = run_l * exp2f(run_m - mn) + sum;
+                            run_m = mn;
+                        }
+                    } else if (MODE == MODE_G) {
+                        T *gp = reinterpret_cast<T *>(a.G) + static_cast<size_t>(grow) * a.ldg + col;
+                        float g[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            float v = exp2f(__uint_as_float(r[j]) * kLog2e - lse2) * inv_nv;
+                            if (col + j == tgt) v -= inv_nv;
+                            g[j] = (col + j < a.vlen) ? v : 0.f;
+                        }
+                        if (sizeof(T) == 2) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(gp);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                dst[q] = make_uint4(pack_bf16x2(g[8 * q + 0], g[8 * q + 1]),
+                                                    pack_bf16x2(g[8 * q + 2], g[8 * q + 3]),
+                                                    pack_bf16x2(g[8 * q + 4], g[8 * q + 5]),
+                                                    pack_bf16x2(g[8 * q + 6], g[8 * q + 7]));
+                        } else {
+                            float4 *dst = reinterpret_cast<float4 *>(gp);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                dst[q] = make_float4(g[4 * q], g[4 * q + 1], g[4 * q + 2], g[4 * q + 3]);
+                        }
+                    } else {
+                        // DW: row = chunk vocab row, out = dW[v0 + row]; DH: row = compacted token
+                        const bool row_ok = (MODE == MODE_DW) ? (grow < a.vlen) : (grow < nv);
+                        if (row_ok && col < a.d) {
+                            float *out = (MODE == MODE_DW)
+                                             ? a.dW + static_cast<size_t>(a.v0 + grow) * a.d + col
+                                             : a.dH_acc + static_cast<size_t>(grow) * a.d + col;
+                            const bool zero_acc = (s.k_blocks == 0);
+                            if (col + 32 <= a.d) {
+                                float4 *o4 = reinterpret_cast<float4 *>(out);
+#pragma unroll
+                                for (int q = 0; q < 8; ++q) {
+                                    float4 v = zero_acc ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                                        : make_float4(__uint_as_float(r[4 * q]),
+                                                                      __uint_as_float(r[4 * q + 1]),
+                                                                      __uint_as_float(r[4 * q + 2]),
+                                                                      __uint_as_float(r[4 * q + 3]));
+                                    if (a.accumulate) {
+                                        const float4 o = o4[q];
+                                        v.x += o.x;
+                                        v.y += o.y;
+                                        v.z += o.z;
+                                        v.w += o.w;
+                                    }
+                                    o4[q] = v;
+                                }
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) {
+                                    if (col + j < a.d) {
+                                        float v = zero_acc ? 0.f : __uint_as_float(r[j]);
+                                        if (a.accumulate) v += out[j];
+                                        out[j] = v;
+                                    }
+                                }
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[acc]);
+            }
+            if (MODE == MODE_LSE && ok && grow < nv)
+                a.part[static_cast<size_t>(sp) * s.m_blocks * kBM + grow] = make_float2(run_m, run_l);
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace lce

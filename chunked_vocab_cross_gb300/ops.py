@@ -1,0 +1,169 @@
+"""Python entry points with the C ABI's names. PyTorch provides device memory
+and the current stream; the arithmetic is all in liblce.so."""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _abi
+
+_DT = {torch.bfloat16: _abi.LCE_BF16, torch.float32: _abi.LCE_FP32}
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _check_inputs(H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor):
+    if not (H.is_cuda and W.is_cuda and targets.is_cuda):
+        raise ValueError("H, W and targets must be CUDA tensors (there is no CPU path)")
+    if H.dtype not in _DT or W.dtype != H.dtype:
+        raise ValueError("H and W must both be bfloat16 or both float32")
+    if targets.dtype != torch.int64:
+        raise ValueError("targets must be int64")
+    if H.dim() != 2 or W.dim() != 2 or targets.dim() != 1:
+        raise ValueError("H must be [N,d], W [V,d], targets [N]")
+    if H.shape[1] != W.shape[1] or H.shape[0] != targets.shape[0]:
+        raise ValueError("shape mismatch between H, W and targets")
+    if not (H.is_contiguous() and W.is_contiguous() and targets.is_contiguous()):
+        raise ValueError("H, W and targets must be contiguous")
+
+
+def workspace_size(N: int, d: int, V: int, dtype=torch.bfloat16, vocab_chunk: int = 0) -> int:
+    return int(_abi.lib().lce_workspace_size(N, d, V, _DT[dtype], vocab_chunk))
+
+
+def lce_run(H, W, targets, ignore_index: int = -100, *, loss=None, dH=None, dW=None, accumulate_dW: bool = False,
+            grad_scale: float = 1.0, lse=None, workspace=None, vocab_chunk: int = 0, stream=None) -> None:
+    """Raw lce_run over caller-provided output tensors."""
+    _check_inputs(H, W, targets)
+    a = _abi.LceArgs()
+    a.dtype = _DT[H.dtype]
+    a.H, a.W, a.targets = H.data_ptr(), W.data_ptr(), targets.data_ptr()
+    a.ignore_index = int(ignore_index)
+    a.N, a.d = H.shape
+    a.V = W.shape[0]
+    a.loss = loss.data_ptr()
+    a.dH = dH.data_ptr() if dH is not None else None
+    a.dW = dW.data_ptr() if dW is not None else None
+    a.accumulate_dW = 1 if accumulate_dW else 0
+    a.grad_scale = float(grad_scale)
+    a.lse = lse.data_ptr() if lse is not None else None
+    if workspace is not None:
+        a.workspace = workspace.data_ptr()
+        a.workspace_bytes = workspace.numel() * workspace.element_size()
+    a.vocab_chunk = int(vocab_chunk)
+    a.stream = _stream(stream)
+    _abi.check(_abi.lib().lce_run(ctypes.byref(a)), "lce_run")
+
+
+def lce_forward(H, W, targets, ignore_index: int = -100, *, return_lse: bool = False, stream=None):
+    """Mean cross-entropy over valid tokens of (H @ W^T, targets); fp32 0-d tensor."""
+    _check_inputs(H, W, targets)
+    loss = torch.empty((), dtype=torch.float32, device=H.device)
+    lse = torch.empty(H.shape[0], dtype=torch.float32, device=H.device) if return_lse else None
+    if H.dtype == torch.bfloat16 and not return_lse:
+        _abi.check(_abi.lib().lce_forward(H.data_ptr(), W.data_ptr(), targets.data_ptr(), int(ignore_index),
+                                          H.shape[0], H.shape[1], W.shape[0], loss.data_ptr(), _stream(stream)),
+                   "lce_forward")
+    else:
+        lce_run(H, W, targets, ignore_index, loss=loss, lse=lse, stream=stream)
+    return (loss, lse) if return_lse else loss
+
+
+def lce_forward_backward(H, W, targets, ignore_index: int = -100, *, dW=None, accumulate_dW: bool = False,
+                         grad_scale: float = 1.0, vocab_chunk: int = 0, return_lse: bool = False,
+                         workspace=None, stream=None):
+    """Loss, dH (H's dtype, zero on ignored rows) and dW (fp32) in one pass."""
+    _check_inputs(H, W, targets)
+    loss = torch.empty((), dtype=torch.float32, device=H.device)
+    dH = torch.empty_like(H)
+    if dW is None:
+        dW = torch.empty(W.shape, dtype=torch.float32, device=W.device)
+        accumulate_dW = False
+    elif dW.dtype != torch.float32 or dW.shape != W.shape or not dW.is_contiguous():
+        raise ValueError("dW must be a contiguous fp32 tensor shaped like W")
+    lse = torch.empty(H.shape[0], dtype=torch.float32, device=H.device) if return_lse else None
+    simple = (H.dtype == torch.bfloat16 and not accumulate_dW and grad_scale == 1.0 and vocab_chunk == 0
+              and not return_lse and workspace is None)
+    if simple:
+        _abi.check(_abi.lib().lce_forward_backward(H.data_ptr(), W.data_ptr(), targets.data_ptr(),
+                                                   int(ignore_index), H.shape[0], H.shape[1], W.shape[0],
+                                                   loss.data_ptr(), dH.data_ptr(), dW.data_ptr(),
+                                                   _stream(stream)),
+                   "lce_forward_backward")
+    else:
+        lce_run(H, W, targets, ignore_index, loss=loss, dH=dH, dW=dW, accumulate_dW=accumulate_dW,
+                grad_scale=grad_scale, lse=lse, workspace=workspace, vocab_chunk=vocab_chunk, stream=stream)
+    out = (loss, dH, dW)
+    return out + (lse,) if return_lse else out
+
+
+def lce_compact(targets, ignore_index: int = -100, V: int | None = None, *, stream=None):
+    """(idx[:Nv] int32, inv int32, Nv, out_of_range) from the compaction kernel."""
+    if not targets.is_cuda or targets.dtype != torch.int64 or targets.dim() != 1:
+        raise ValueError("targets must be a 1-D int64 CUDA tensor")
+    targets = targets.contiguous()
+    N = targets.shape[0]
+    idx = torch.empty(N, dtype=torch.int32, device=targets.device)
+    inv = torch.empty(N, dtype=torch.int32, device=targets.device)
+    counts = torch.empty(2, dtype=torch.int32, device=targets.device)
+    _abi.check(_abi.lib().lce_compact(targets.data_ptr(), N, int(ignore_index), int(V if V else 2**31 - 1),
+                                      idx.data_ptr(), inv.data_ptr(), counts.data_ptr(), _stream(stream)),
+               "lce_compact")
+    nv, bad = counts.tolist()
+    return idx[:nv], inv, nv, bad
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status bits."""
+    bits = ctypes.c_int32(0)
+    _abi.lib().lce_get_device_status(_stream(stream), ctypes.byref(bits))
+    return int(bits.value)
+
+
+def launch_count() -> int:
+    return int(_abi.lib().lce_launch_count())
+
+
+def profile_begin() -> None:
+    _abi.check(_abi.lib().lce_profile_begin(), "lce_profile_begin")
+
+
+def profile_end() -> dict:
+    n = _abi.PROFILE_PHASES
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    _abi.check(_abi.lib().lce_profile_end(ms, cnt, n), "lce_profile_end")
+    return {name: {"ms": ms[i], "launches": int(cnt[i])} for i, name in enumerate(_abi.PHASE_NAMES)}
+
+
+class _LinearCrossEntropy(torch.autograd.Function):
+    """Training use: the forward call already produces dH and dW (the logits are
+    recomputed inside it, never stored); backward scales them by the incoming
+    scalar gradient."""
+
+    @staticmethod
+    def forward(ctx, H, W, targets, ignore_index):
+        loss, dH, dW = lce_forward_backward(H.contiguous(), W.contiguous(), targets.contiguous(), ignore_index)
+        ctx.save_for_backward(dH, dW)
+        ctx.w_dtype = W.dtype
+        return loss
+
+    @staticmethod
+    def backward(ctx, g):
+        dH, dW = ctx.saved_tensors
+        gH = dH if ctx.needs_input_grad[0] else None
+        gW = dW if ctx.needs_input_grad[1] else None
+        if gH is not None:
+            gH = (gH.float() * g).to(dH.dtype)
+        if gW is not None:
+            gW = (gW * g).to(ctx.w_dtype)
+        return gH, gW, None, None
+
+
+def linear_cross_entropy(H, W, targets, ignore_index: int = -100):
+    """loss = cross_entropy(H @ W^T, targets, ignore_index) without materialising logits."""
+    return _LinearCrossEntropy.apply(H, W, targets, ignore_index)

@@ -1,0 +1,179 @@
+/*
+ * lce.h — C ABI of the fused output-projection + cross-entropy library
+ * (liblce.so, sm_103a).
+ *
+ * Operation. For hidden states H[N,d], a vocabulary matrix W[V,d] (tied to the
+ * input embedding or not) and integer targets t[N] in which ignore_index marks
+ * padding, with I = { i : t_i != ignore_index } and Nv = |I|:
+ *
+ *   loss    = (1/Nv) * sum_{i in I} ( logsumexp_v(h_i . w_v) - h_i . w_{t_i} )
+ *   dH[i,:] = sum_v g_iv W[v,:]  for i in I, and 0 for ignored rows
+ *   dW[v,:] = sum_{i in I} g_iv H[i,:]
+ *   g_iv    = ( softmax_v(h_i . W^T)_v - [v == t_i] ) / Nv
+ *
+ * This is the output projection and loss computed in streamed chunks with
+ * padding tokens skipped, so that no N x V logits buffer ever exists
+ * ("OjasX 0.6.1: Training a 1B-Parameter LLM in 6.35GB of RAM", section
+ * "Core Technology", the zero-byte vocabulary logits item), with the logits
+ * recomputed in backward rather than kept ("6GB显卡预训练11亿参数模型：全是已发表
+ * 技术，实测需375天", section "关键参数说明", --chunked-loss 512, and section
+ * "内存实际花在哪里"). The row normaliser is the streaming (online) softmax
+ * recurrence, which reaches the same value as the two-pass one (OjasX page,
+ * "Online Softmax" note). Padding is removed by an on-device compaction into a
+ * dense index list ("为什么26万词表会卡死16GB显卡", section 2.3 稀疏索引引擎).
+ *
+ * Conventions shared by every entry point.
+ *  - All tensor arguments are DEVICE pointers owned by the caller, row-major
+ *    and contiguous; the library never frees or retains them after the call.
+ *  - H, W (and dH) are bf16 for lce_forward / lce_forward_backward, or the
+ *    dtype given in lce_args_t; dW, loss and lse are fp32.
+ *  - H, W, dH, dW base pointers must be 16-byte aligned and d*sizeof(elem)
+ *    a multiple of 16 (d % 8 == 0 for bf16, d % 4 == 0 for fp32): W and the
+ *    compacted H are read by the Tensor Memory Accelerator.
+ *  - 1 <= N < 2^31, 1 <= d <= 65536, 1 <= V < 2^31.
+ *  - Work is enqueued on `stream` (NULL = the legacy default stream) and the
+ *    call returns without synchronising. Scratch memory is stream-ordered
+ *    (cudaMallocAsync/cudaFreeAsync) unless a workspace is passed.
+ *  - Host-detectable problems (null pointers, shapes, alignment, device)
+ *    return an error code synchronously and enqueue nothing. Problems only the
+ *    device can see (a non-ignored target outside [0, V), a bounded wait that
+ *    gave up) never trap: they set bits in a per-device status word that
+ *    lce_get_device_status reads; the loss is then NaN and the gradients are
+ *    unspecified.
+ *  - Nv == 0 gives loss = NaN (a mean over no tokens) and zero dH and dW.
+ *  - Results are deterministic: the same inputs give bitwise-identical
+ *    outputs (no floating-point atomics).
+ *  - The library runs on sm_103 devices only (LCE_ERR_DEVICE otherwise).
+ */
+#ifndef LCE_H
+#define LCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st *lce_stream_t;
+
+typedef enum {
+    LCE_OK = 0,
+    LCE_ERR_NULL = 1,         /* a required pointer is NULL */
+    LCE_ERR_SHAPE = 2,        /* N, d, V or vocab_chunk out of range */
+    LCE_ERR_ALIGN = 3,        /* base pointer or row stride not 16-byte aligned */
+    LCE_ERR_DTYPE = 4,        /* unknown dtype */
+    LCE_ERR_CUDA = 5,         /* a CUDA call failed; see lce_last_cuda_error() */
+    LCE_ERR_WORKSPACE = 6,    /* workspace_bytes below lce_workspace_size() */
+    LCE_ERR_TARGET_RANGE = 7, /* device: a non-ignored target outside [0, V) */
+    LCE_ERR_TIMEOUT = 8,      /* device: a bounded wait inside a kernel gave up */
+    LCE_ERR_DEVICE = 9        /* current device is not sm_103 */
+} lce_status_t;
+
+typedef enum { LCE_BF16 = 0, LCE_FP32 = 1 } lce_dtype_t;
+
+/* Bits of the device status word (lce_get_device_status). */
+#define LCE_DEV_TARGET_RANGE 0x1  /* a non-ignored target was outside [0, V) */
+#define LCE_DEV_TIMEOUT      0x2  /* a pipeline wait gave up; that kernel returned early */
+
+/*
+ * Forward only: writes the mean loss to the device scalar `loss`.
+ * H [N,d] bf16, W [V,d] bf16, targets [N] int64.
+ */
+lce_status_t lce_forward(const void *H, const void *W, const int64_t *targets,
+                         int64_t ignore_index, int64_t N, int64_t d, int64_t V,
+                         float *loss, lce_stream_t stream);
+
+/*
+ * Forward and backward in one call: loss (device fp32 scalar), dH [N,d] bf16
+ * (overwritten; ignored rows are zero) and dW [V,d] fp32 (overwritten).
+ * H, W and targets as in lce_forward. dW is fp32 so a tied W's gradient can be
+ * added to the input-embedding gradient without a rounding step.
+ */
+lce_status_t lce_forward_backward(const void *H, const void *W, const int64_t *targets,
+                                  int64_t ignore_index, int64_t N, int64_t d, int64_t V,
+                                  float *loss, void *dH, float *dW, lce_stream_t stream);
+
+/*
+ * Valid-token compaction alone (the first step of every call): idx[0..Nv)
+ * receives the ascending positions whose target is not ignore_index, inv[i]
+ * the compacted row of position i or -1, counts[0] = Nv and counts[1] = the
+ * number of non-ignored targets outside [0, V). idx and inv hold N int32
+ * each, counts 2 int32; all device pointers. One CTA sweeps the targets with
+ * warp ballots and a block scan; the list is exact (integer) and ascending.
+ * Padding-aware valid mask of "为什么26万词表会卡死16GB显卡", section 2.3
+ * 稀疏索引引擎.
+ */
+lce_status_t lce_compact(const int64_t *targets, int64_t N, int64_t ignore_index, int64_t V,
+                         int32_t *idx, int32_t *inv, int32_t *counts, lce_stream_t stream);
+
+/* Full argument set for lce_run. Zero-initialise, then fill. */
+typedef struct {
+    lce_dtype_t dtype;        /* element type of H, W and dH */
+    const void *H;            /* [N,d] */
+    const void *W;            /* [V,d] */
+    const int64_t *targets;   /* [N] */
+    int64_t ignore_index;
+    int64_t N, d, V;
+    float *loss;              /* required: device fp32 scalar */
+    void *dH;                 /* [N,d] of dtype, or NULL for forward only */
+    float *dW;                /* [V,d] fp32, or NULL for forward only (NULL iff dH is NULL) */
+    int accumulate_dW;        /* nonzero: dW += gradient; zero: dW = gradient */
+    float grad_scale;         /* multiplies dH and dW (0 is read as 1) */
+    float *lse;               /* optional [N] fp32: per-row logsumexp (natural log), NaN on ignored rows */
+    void *workspace;          /* optional device scratch; NULL = stream-ordered allocation */
+    size_t workspace_bytes;   /* size of `workspace` */
+    int64_t vocab_chunk;      /* vocab rows per backward chunk; 0 = default; else a multiple of 256 */
+    lce_stream_t stream;
+} lce_args_t;
+
+/* Forward, or forward + backward when dH/dW are given, with every option. */
+lce_status_t lce_run(const lce_args_t *args);
+
+/*
+ * Bytes of scratch lce_run needs for these sizes (what the library allocates
+ * itself when no workspace is passed). Grows as O(N*(d + vocab_chunk)), never
+ * with N*V. Returns 0 for invalid arguments.
+ */
+size_t lce_workspace_size(int64_t N, int64_t d, int64_t V, lce_dtype_t dtype, int64_t vocab_chunk);
+
+/*
+ * Synchronises `stream`, then returns in *bits the current device's status
+ * word (LCE_DEV_* bits accumulated since the last read) and clears it.
+ * Returns LCE_ERR_TARGET_RANGE or LCE_ERR_TIMEOUT when the matching bit is
+ * set, LCE_OK when the word is clear.
+ */
+lce_status_t lce_get_device_status(lce_stream_t stream, int32_t *bits);
+
+/* Static string naming a status code. */
+const char *lce_status_string(lce_status_t status);
+
+/* cudaError_t value of the last CUDA failure seen by this thread (0 = none). */
+int lce_last_cuda_error(void);
+
+/* Number of kernels this library has launched in this process. */
+int64_t lce_launch_count(void);
+
+/*
+ * Phase timing for profiling. While enabled (on the calling thread), every
+ * call records CUDA events on its stream around each phase:
+ *   0 compaction + gather of valid rows, 1 logits + online log-sum-exp,
+ *   2 log-sum-exp merge + loss, 3 backward logits -> G, 4 dW = G^T H,
+ *   5 dH = G W (+ scatter to dH).
+ * lce_profile_end synchronises those events and returns, per phase, the summed
+ * milliseconds and the number of kernel launches; it then disables timing.
+ * n is the length of both output arrays (at most LCE_PROFILE_PHASES used).
+ */
+#define LCE_PROFILE_PHASES 6
+lce_status_t lce_profile_begin(void);
+lce_status_t lce_profile_end(double *ms, int64_t *launches, int n);
+
+/* ABI version: major*10000 + minor*100 + patch. */
+int lce_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LCE_H */

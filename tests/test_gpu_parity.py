@@ -1,0 +1,219 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle on seeded
+inputs: element by element at sizes the oracle finishes in seconds (several
+tiles plus ragged tails), and edge cases. Tolerances: |loss| <= 1e-3 and
+relative Frobenius error <= 5e-3 for dH and dW on bf16 inputs."""
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import chunked_vocab_cross_gb300 as lce  # noqa: E402
+import oracle  # noqa: E402
+from lce_testutil import TOL_LOSS, TOL_LSE, TOL_REL, np64, rel_fro, to_device  # noqa: E402
+from synth_inputs import IGNORE_INDEX, WORKLOADS, make_inputs, make_targets  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from chunked_vocab_cross_gb300.build import build
+    build()
+    lce.device_status()   # clear the status word
+    yield
+
+
+def _run_and_compare(x, vocab_chunk=0, tol_loss=TOL_LOSS, tol_rel=TOL_REL, tol_lse=TOL_LSE):
+    H, W, t = to_device(x)
+    loss, dH, dW, lse = lce.lce_forward_backward(H, W, t, IGNORE_INDEX, vocab_chunk=vocab_chunk, return_lse=True)
+    torch.cuda.synchronize()
+    assert lce.device_status() == 0
+    ref = oracle.forward_backward(x.H_f32(), x.W_f32(), x.targets, IGNORE_INDEX)
+    valid = x.targets != IGNORE_INDEX
+    lse_g = np64(lse)
+    errs = {
+        "loss": abs(loss.item() - ref["loss"]),
+        "lse": float(np.max(np.abs(lse_g[valid] - ref["lse"]))) if valid.any() else 0.0,
+        "dH": rel_fro(np64(dH), ref["dH"]),
+        "dW": rel_fro(np64(dW), ref["dW"]),
+    }
+    print(x.workload, errs)
+    assert np.all(np.isnan(lse_g[~valid]))
+    assert np.all(np64(dH)[~valid] == 0.0)
+    assert errs["loss"] <= tol_loss, errs
+    assert errs["lse"] <= tol_lse, errs
+    assert errs["dH"] <= tol_rel, errs
+    assert errs["dW"] <= tol_rel, errs
+    return errs
+
+
+# ------------------------------------------------------------------ compaction
+
+def _compaction_cases():
+    g = np.random.default_rng(0)
+    cases = []
+    for name, w in WORKLOADS.items():
+        cases.append((name, make_targets(w), w.V))
+    for n in (1, 31, 32, 33, 1023, 1024, 1025, 5000):
+        t = g.integers(0, 100, n)
+        t[g.random(n) < 0.37] = IGNORE_INDEX
+        cases.append((f"rand{n}", t, 100))
+    cases.append(("all_ignored", np.full(77, IGNORE_INDEX), 10))
+    cases.append(("none_ignored", np.arange(2049) % 10, 10))
+    t = np.array([5, IGNORE_INDEX, 10, -1, 9, 12, IGNORE_INDEX, 0])
+    cases.append(("out_of_range", t, 10))
+    return cases
+
+
+@pytest.mark.parametrize("case", _compaction_cases(), ids=lambda c: c[0])
+def test_compaction_bit_exact(case):
+    _, t, V = case
+    idx, inv, nv, bad = lce.lce_compact(torch.from_numpy(t).cuda(), IGNORE_INDEX, V)
+    expect = oracle.valid_rows(t, IGNORE_INDEX)
+    assert nv == len(expect)
+    np.testing.assert_array_equal(idx.cpu().numpy(), expect)
+    inv_expect = np.full(len(t), -1)
+    inv_expect[expect] = np.arange(len(expect))
+    np.testing.assert_array_equal(inv.cpu().numpy(), inv_expect)
+    assert bad == oracle.out_of_range_targets(t, IGNORE_INDEX, V)
+    lce.device_status()
+
+
+# ------------------------------------------------------------- small parity
+
+SMALL = [
+    # (N, d, V, padding)   chosen to span several 128x256 tiles and ragged tails
+    (1, 64, 1000, ("none",)),
+    (127, 64, 1000, ("random_frac", 0.0)),
+    (129, 128, 513, ("random_frac", 0.2)),
+    (300, 128, 1000, ("random_frac", 0.1)),
+    (256, 64, 1000, ("random_frac", 0.1)),
+    (700, 200, 4099, ("random_frac", 0.3)),
+    (1000, 256, 3000, ("random_frac", 0.5)),
+    (640, 512, 8192, ("trailing_frac", 0.25)),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: f"N{s[0]}_d{s[1]}_V{s[2]}")
+def test_small_bf16_parity(shape):
+    N, d, V, pad = shape
+    x = make_inputs("gpt1b", N=N, d=d, V=V, padding=pad, seqs=1)
+    _run_and_compare(x)
+
+
+@pytest.mark.parametrize("vocab_chunk", [256, 768, 1024])
+def test_vocab_chunk_sizes(vocab_chunk):
+    x = make_inputs("gpt1b", N=500, d=256, V=2900, padding=("random_frac", 0.2), seqs=1)
+    _run_and_compare(x, vocab_chunk=vocab_chunk)
+
+
+def test_tiny_workload_bf16_rounded():
+    """The tiny workload's shapes with bf16 inputs (the fp32 path has its own test)."""
+    w = WORKLOADS["tiny"].with_(dtype="bf16")
+    _run_and_compare(make_inputs(w))
+
+
+def test_all_ignored_gives_nan_and_zero_grads():
+    x = make_inputs("gpt1b", N=200, d=64, V=700, padding=("all",), seqs=1)
+    H, W, t = to_device(x)
+    loss, dH, dW = lce.lce_forward_backward(H, W, t, IGNORE_INDEX)
+    torch.cuda.synchronize()
+    assert math.isnan(loss.item())
+    assert torch.count_nonzero(dH).item() == 0
+    assert torch.count_nonzero(dW).item() == 0
+    assert lce.device_status() == 0
+
+
+def test_forward_only_matches_oracle():
+    x = make_inputs("gpt1b", N=400, d=128, V=2000, padding=("random_frac", 0.15), seqs=1)
+    H, W, t = to_device(x)
+    loss = lce.lce_forward(H, W, t, IGNORE_INDEX)
+    ref = oracle.forward(x.H_f32(), x.W_f32(), x.targets, IGNORE_INDEX)
+    assert abs(loss.item() - ref["loss"]) <= TOL_LOSS
+
+
+def test_out_of_range_target_sets_status_and_nan():
+    x = make_inputs("gpt1b", N=64, d=64, V=500, padding=("none",), seqs=1)
+    x.targets[7] = 500
+    H, W, t = to_device(x)
+    loss, dH, dW = lce.lce_forward_backward(H, W, t, IGNORE_INDEX)
+    bits = lce.device_status()
+    assert bits & 0x1
+    assert math.isnan(loss.item())
+
+
+def test_deterministic_bitwise():
+    x = make_inputs("gpt1b", N=1500, d=512, V=6000, padding=("random_frac", 0.3), seqs=1)
+    H, W, t = to_device(x)
+    a = lce.lce_forward_backward(H, W, t, IGNORE_INDEX)
+    b = lce.lce_forward_backward(H, W, t, IGNORE_INDEX)
+    torch.cuda.synchronize()
+    for u, v in zip(a, b):
+        assert torch.equal(u.view(torch.int8) if u.dim() else u, v.view(torch.int8) if v.dim() else v)
+
+
+def test_accumulate_dW_and_grad_scale():
+    x = make_inputs("gpt1b", N=300, d=128, V=1500, padding=("random_frac", 0.1), seqs=1)
+    H, W, t = to_device(x)
+    base = torch.randn(W.shape, device="cuda", dtype=torch.float32)
+    dW = base.clone()
+    loss, dH, dW = lce.lce_forward_backward(H, W, t, IGNORE_INDEX, dW=dW, accumulate_dW=True, grad_scale=0.5)
+    torch.cuda.synchronize()
+    ref = oracle.forward_backward(x.H_f32(), x.W_f32(), x.targets, IGNORE_INDEX)
+    assert rel_fro(np64(dW - base), 0.5 * ref["dW"]) <= TOL_REL
+    assert rel_fro(np64(dH), 0.5 * ref["dH"]) <= TOL_REL
+
+
+def test_autograd_function():
+    x = make_inputs("gpt1b", N=200, d=64, V=900, padding=("random_frac", 0.1), seqs=1)
+    H, W, t = to_device(x)
+    H.requires_grad_(True)
+    W.requires_grad_(True)
+    loss = lce.linear_cross_entropy(H, W, t, IGNORE_INDEX)
+    (2.0 * loss).backward()
+    ref = oracle.forward_backward(x.H_f32(), x.W_f32(), x.targets, IGNORE_INDEX)
+    assert abs(loss.item() - ref["loss"]) <= TOL_LOSS
+    assert rel_fro(np64(H.grad), 2 * ref["dH"]) <= 1e-2      # grads rounded to bf16 on return
+    assert rel_fro(np64(W.grad), 2 * ref["dW"]) <= 1e-2
+
+
+def test_canaries_untouched():
+    """Outputs sit inside larger buffers filled with a sentinel; nothing outside
+    the output ranges may change (bounds check without compute-sanitizer)."""
+    x = make_inputs("gpt1b", N=333, d=136, V=1234, padding=("random_frac", 0.2), seqs=1)
+    H, W, t = to_device(x)
+    N, d, V = 333, 136, 1234
+    pad = 4096
+    dh_buf = torch.full((N * d + 2 * pad,), 7.0, device="cuda", dtype=torch.bfloat16)
+    dw_buf = torch.full((V * d + 2 * pad,), 7.0, device="cuda", dtype=torch.float32)
+    loss_buf = torch.full((2 * pad + 1,), 7.0, device="cuda", dtype=torch.float32)
+    lse_buf = torch.full((N + 2 * pad,), 7.0, device="cuda", dtype=torch.float32)
+    dH = dh_buf[pad:pad + N * d].view(N, d)
+    dW = dw_buf[pad:pad + V * d].view(V, d)
+    loss = loss_buf[pad]
+    lse = lse_buf[pad:pad + N]
+    lce.lce_run(H, W, t, IGNORE_INDEX, loss=loss, dH=dH, dW=dW, lse=lse)
+    torch.cuda.synchronize()
+    for buf, n in ((dh_buf, N * d), (dw_buf, V * d), (loss_buf, 1), (lse_buf, N)):
+        assert torch.all(buf[:pad] == 7.0) and torch.all(buf[pad + n:] == 7.0)
+    ref = oracle.forward_backward(x.H_f32(), x.W_f32(), x.targets, IGNORE_INDEX)
+    assert abs(loss.item() - ref["loss"]) <= TOL_LOSS
+    assert rel_fro(np64(dW), ref["dW"]) <= TOL_REL
+
+
+def test_caller_workspace_and_size():
+    x = make_inputs("gpt1b", N=400, d=128, V=1500, padding=("random_frac", 0.1), seqs=1)
+    H, W, t = to_device(x)
+    n = lce.workspace_size(400, 128, 1500)
+    assert 0 < n < 400 * 1500 * 4 * 4
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    loss, dH, dW = lce.lce_forward_backward(H, W, t, IGNORE_INDEX, workspace=ws)
+    ref = oracle.forward_backward(x.H_f32(), x.W_f32(), x.targets, IGNORE_INDEX)
+    assert abs(loss.item() - ref["loss"]) <= TOL_LOSS
+    small = torch.empty(n - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(lce.LceError):
+        lce.lce_forward_backward(H, W, t, IGNORE_INDEX, workspace=small)
