@@ -1,0 +1,345 @@
+"""Benchmark of the fused output-projection + cross-entropy forward+backward.
+
+One step = one lce_forward_backward over the whole batch of the workload
+(compaction, logits + online log-sum-exp, loss, recomputed logits -> G, dW, dH).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload llama8b] [--impl lce|reference]
+
+Prints one JSON line (rank 0). `value` is valid tokens/s with inputs resident in
+HBM; `e2e` is the same metric through the public call with H and targets copied
+from pinned host memory and the loss read back every step (W, the weight
+matrix, stays resident as in training). Under torchrun each rank runs its own
+batch (independent problems, no collective): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused linear-CE fwd+bwd valid tokens/sec; % of dense BF16 tensor peak"
+UNIT = "valid tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clocks unavailable"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for _, _, flags in rows for n, f in zip(names, flags) if f.lower() == "active"})
+        return {"sm_mhz": float(np.median([r[0] for r in rows])), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup(gpus: int):
+    import torch
+    rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t)
+    return float(t.item())
+
+
+def cpu_oracle_rate(x, budget_s: float):
+    """The fp64 oracle, as it stands, on the first valid rows of the batch
+    (full V and d, forward + backward), grown batch by batch until `budget_s`."""
+    import oracle
+    valid = np.nonzero(x.targets != -100)[0]
+    # input preparation, outside the timed loop: exact float64 copies of H and W
+    H = x.H_f32()[valid[:8192]].astype(np.float64)
+    W = x.W_f32().astype(np.float64)
+    tv = x.targets[valid[:8192]]
+    rows, t0, step = 0, time.perf_counter(), 128
+    while rows < len(tv):
+        oracle.forward_backward(H[rows:rows + step], W, tv[rows:rows + step], -100)
+        rows += len(tv[rows:rows + step])
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0))
+    return rows / el, el, rows, cores
+
+
+def workload_desc(x, nv):
+    w = x.workload
+    return {"workload": f"{w.name}: N={w.N} ({w.seqs}x{w.N // w.seqs}), d={w.d}, V={w.V}, Nv={nv}, {w.dtype}, "
+                        f"targets {w.targets}, padding {w.padding}, W~N(0,1/d)*{w.w_scale}, seed {w.seed}",
+            "N": w.N, "d": w.d, "V": w.V, "n_valid": int(nv),
+            "l2": "inputs larger than L2 (W alone %.2f GB > 129 MB L2); no flush needed" % (w.V * w.d * 2 / 1e9)}
+
+
+def run_reference(args):
+    rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+    if rank != 0:
+        return
+    from synth_inputs import make_inputs
+    x = make_inputs(args.workload)
+    nv = int((x.targets != -100).sum())
+    budget = float(os.environ.get("LCE_REF_STEP_S", "6"))
+    times, rows_done = [], 0
+    for _ in range(args.warmup):
+        cpu_oracle_rate(x, budget / 4)
+    for _ in range(args.steps):
+        rate, el, rows, cores = cpu_oracle_rate(x, budget)
+        times.append(el)
+        rows_done += rows
+    value = rows_done / sum(times)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * nv / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_desc(x, nv),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"each step: the first valid rows of the batch (about {budget:.0f} s of "
+                                       f"fp64 oracle fwd+bwd over full V and d), rate scaled to valid tokens/s"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="llama8b")
+    ap.add_argument("--impl", default="lce", choices=["lce", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+
+    import chunked_vocab_cross_gb300 as lce
+    from chunked_vocab_cross_gb300.build import build
+    from synth_inputs import make_inputs
+
+    rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        build()
+    barrier(world)
+
+    # each rank draws its own batch (seed = rank): independent problems
+    x = make_inputs(args.workload, seed=rank)
+    nv = int((x.targets != -100).sum())
+    w = x.workload
+    H_host = torch.from_numpy(x.H.view(np.int16)).view(torch.bfloat16).pin_memory()
+    t_host = torch.from_numpy(x.targets).pin_memory()
+    H = H_host.to(dev)
+    W = torch.from_numpy(x.W.view(np.int16)).view(torch.bfloat16).to(dev)
+    t = t_host.to(dev)
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    dH = torch.empty_like(H)
+    dW = torch.empty(W.shape, dtype=torch.float32, device=dev)
+    ws = torch.empty(lce.workspace_size(w.N, w.d, w.V), dtype=torch.uint8, device=dev)
+
+    def step():
+        lce.lce_run(H, W, t, -100, loss=loss, dH=dH, dW=dW, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    lce.device_status()
+
+    # ------------------------------------------------------------ timed region
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    l0 = lce.launch_count()
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    launches = (lce.launch_count() - l0) // max(1, args.steps) * args.steps
+    ms_step = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
+    status = lce.device_status()
+    nv_all = sum_over_ranks(nv, world)
+    value = nv_all / (ms_step / 1e3)
+
+    # -------------------------------------------- per-phase events (roofline)
+    lce.profile_begin()
+    prof_steps = max(3, min(args.steps, 10))
+    for _ in range(prof_steps):
+        step()
+    phases = lce.profile_end()
+    torch.cuda.synchronize()
+
+    # ------------------------------------------------ end to end (host buffers)
+    e2e_loss = torch.empty((), dtype=torch.float32).pin_memory()
+    H_e = torch.empty_like(H)
+    t_e = torch.empty_like(t)
+
+    def e2e_step():
+        H_e.copy_(H_host, non_blocking=True)
+        t_e.copy_(t_host, non_blocking=True)
+        l, _, _ = lce.lce_forward_backward(H_e, W, t_e, -100)
+        e2e_loss.copy_(l, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    useful_flops = 6.0 * nv * w.d * w.V
+    executed_flops = 8.0 * nv * w.d * w.V
+    tflops_useful = useful_flops / (ms_step / 1e3) / 1e12 * 1.0
+    # dominant kernel: largest share of the profiled step time
+    gemm_phases = {"logits_lse": 1, "bwd_logits_G": 1, "dW": 1, "dH": 1}
+    name = max(gemm_phases, key=lambda k: phases[k]["ms"])
+    ph = phases[name]
+    per_launch_ms = ph["ms"] / max(1, ph["launches"])
+    if name == "logits_lse":
+        flops_launch = 2.0 * nv * w.d * w.V
+    else:
+        # one launch per vocab chunk
+        n_chunks = -(-w.V // 4096)
+        kern_launches = n_chunks * prof_steps
+        per_launch_ms = ph["ms"] / kern_launches
+        flops_launch = 2.0 * nv * w.d * w.V / n_chunks
+    achieved = flops_launch / (per_launch_ms / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    total_prof = sum(p["ms"] for p in phases.values())
+    cpu = None
+    if not args.no_cpu_baseline:
+        rate, el, rows, cores = cpu_oracle_rate(x, args.cpu_budget)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"first {rows} valid rows of the batch, fp64 oracle forward+backward over full "
+                         f"V={w.V} and d={w.d} ({el:.1f} s), scaled to valid tokens/s"}
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_desc(x, nv),
+        "pct_dense_bf16_peak": {
+            "useful_tflops": tflops_useful,
+            "of_burst": tflops_useful / float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
+            "of_sustained": tflops_useful / peak, "peaks": peak_src,
+            "note": "useful FLOPs = 6*Nv*d*V; the path executes 8*Nv*d*V (logits recomputed in backward)"},
+        "roofline": {"bound": "tensor", "kernel": f"k_gemm ({name})", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "peak_kind": f"bf16_tflops_sustained ({peak_src})",
+                     "flops_per_launch": flops_launch, "ms_per_launch": per_launch_ms},
+        "phases_ms_per_step": {k: v["ms"] / prof_steps for k, v in phases.items()},
+        "phase_share": {k: (v["ms"] / total_prof if total_prof else None) for k, v in phases.items()},
+        "cpu_baseline": cpu,
+        "e2e": {"value": nv / (e2e_ms / 1e3) * world, "unit": UNIT,
+                "h2d_bytes_per_step": int(H.numel() * 2 + t.numel() * 8), "d2h_bytes_per_step": 4,
+                "resident": "W (weights)", "ms_per_step": e2e_ms},
+        "gpu_launches": int(launches),
+        "device_status": status,
+        "clocks": clocks,
+        "workspace_bytes": int(ws.numel()),
+        "logits_bytes_avoided": int(w.N * w.V * 4),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -359,7 +359,7 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
         }
     }
     {
-        PhaseScope ph(5, st);
+        PhaseScope ph(6, st);
         const int grid = N < 8 * di.sms ? N : 8 * di.sms;
         k_dh_scatter<T><<<grid, 256, 0, st>>>(dHacc, inv, N, d, static_cast<T *>(a->dH));
         LCE_CHECK_LAUNCH();

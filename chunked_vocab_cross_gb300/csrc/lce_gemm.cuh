@@ -358,7 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int grow = mb * kBM + trow;      // compacted row (LSE/G/DH) or chunk vocab row (DW)
             int tgt = -1;
             float lse2 = 0.f;
-            if (MODE == MODE_LSE || MODE == MODE_G) tgt = grow < nv ? a.tc[grow] : -1;
+            // target column relative to the first column this launch covers (the
+            // chunk start v0 in MODE_G), -1 / out of range when absent
+            if (MODE == MODE_LSE || MODE == MODE_G) tgt = grow < nv ? a.tc[grow] - a.v0 : -1;
             if (MODE == MODE_G) lse2 = grow < nv ? a.lse2[grow] : INFINITY;
             float run_m = -INFINITY, run_l = 0.f;
             for (int nt = n0; nt < n1; ++nt, ++tile) {

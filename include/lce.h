@@ -160,12 +160,12 @@ int64_t lce_launch_count(void);
  * call records CUDA events on its stream around each phase:
  *   0 compaction + gather of valid rows, 1 logits + online log-sum-exp,
  *   2 log-sum-exp merge + loss, 3 backward logits -> G, 4 dW = G^T H,
- *   5 dH = G W (+ scatter to dH).
+ *   5 dH accumulation G W, 6 scatter of dH to the caller's rows.
  * lce_profile_end synchronises those events and returns, per phase, the summed
  * milliseconds and the number of kernel launches; it then disables timing.
  * n is the length of both output arrays (at most LCE_PROFILE_PHASES used).
  */
-#define LCE_PROFILE_PHASES 6
+#define LCE_PROFILE_PHASES 7
 lce_status_t lce_profile_begin(void);
 lce_status_t lce_profile_end(double *ms, int64_t *launches, int n);
 

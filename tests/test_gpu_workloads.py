@@ -1,0 +1,114 @@
+"""Parity on the five workloads at full size, in the launch configuration the
+benchmark times (lce_run with a caller workspace):
+  tiny        fp32 inputs (tf32 tensor-core path), full oracle
+  gpt1b       full oracle (every row, every gradient entry)
+  smallvocab  full oracle
+  llama8b     full loss and every row's lse; dH on 256 seeded token rows and
+              dW on 256 seeded vocab rows
+  vocab256k   same sampling as llama8b
+Tolerances: bf16 inputs |loss| <= 1e-3, relative Frobenius <= 5e-3 for dH and
+dW, per-row lse <= 1e-3 (diagnostic). fp32 inputs run on tf32 tensor cores
+(10 explicit mantissa bits): |loss| <= 2e-3, lse <= 5e-3, dH/dW <= 1e-2."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import chunked_vocab_cross_gb300 as lce  # noqa: E402
+import oracle  # noqa: E402
+from lce_testutil import TOL_LOSS, TOL_LSE, TOL_REL, np64, rel_fro, to_device  # noqa: E402
+from synth_inputs import IGNORE_INDEX, make_inputs  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from chunked_vocab_cross_gb300.build import build
+    build()
+    lce.device_status()
+    yield
+
+
+def _gpu_run(x):
+    H, W, t = to_device(x)
+    w = x.workload
+    ws = torch.empty(lce.workspace_size(w.N, w.d, w.V, H.dtype), dtype=torch.uint8, device="cuda")
+    loss, dH, dW, lse = lce.lce_forward_backward(H, W, t, IGNORE_INDEX, workspace=ws, return_lse=True)
+    torch.cuda.synchronize()
+    assert lce.device_status() == 0
+    out = {"loss": loss.item(), "lse": np64(lse), "dH": dH, "dW": dW}
+    del H, W, ws
+    return out
+
+
+@pytest.mark.parametrize("name", ["gpt1b", "smallvocab"])
+def test_full_oracle(name):
+    x = make_inputs(name)
+    g = _gpu_run(x)
+    ref = oracle.forward_backward(x.H_f32().astype(np.float64), x.W_f32().astype(np.float64), x.targets,
+                                  IGNORE_INDEX)
+    valid = x.targets != IGNORE_INDEX
+    dH = np64(g["dH"])
+    errs = {"loss": abs(g["loss"] - ref["loss"]),
+            "lse": float(np.max(np.abs(g["lse"][valid] - ref["lse"]))),
+            "dH": rel_fro(dH, ref["dH"]), "dW": rel_fro(np64(g["dW"]), ref["dW"])}
+    print(name, errs)
+    assert np.all(dH[~valid] == 0.0)
+    assert errs["loss"] <= TOL_LOSS and errs["lse"] <= TOL_LSE, errs
+    assert errs["dH"] <= TOL_REL and errs["dW"] <= TOL_REL, errs
+
+
+@pytest.mark.parametrize("name", ["llama8b", "vocab256k"])
+def test_sampled_oracle(name):
+    x = make_inputs(name)
+    g = _gpu_run(x)
+    rng = np.random.default_rng(1234)
+    rows = np.sort(rng.choice(x.workload.N, 256, replace=False))
+    vocab = np.sort(rng.choice(x.workload.V, 256, replace=False))
+    # exact float64 copies of the inputs, made once (the oracle widens per block otherwise)
+    ref = oracle.sampled_reference(x.H_f32().astype(np.float64), x.W_f32().astype(np.float64), x.targets,
+                                   IGNORE_INDEX, rows, vocab)
+    valid = x.targets != IGNORE_INDEX
+    dH_rows = np64(g["dH"][torch.from_numpy(rows).cuda()])
+    dW_rows = np64(g["dW"][torch.from_numpy(vocab).cuda()])
+    errs = {"loss": abs(g["loss"] - ref["loss"]),
+            "lse": float(np.max(np.abs(g["lse"][valid] - ref["lse"]))),
+            "dH_rows": rel_fro(dH_rows, ref["dH_rows"]), "dW_rows": rel_fro(dW_rows, ref["dW_rows"])}
+    print(name, errs)
+    assert np.all(dH_rows[~valid[rows]] == 0.0)
+    assert errs["loss"] <= TOL_LOSS and errs["lse"] <= TOL_LSE, errs
+    assert errs["dH_rows"] <= TOL_REL and errs["dW_rows"] <= TOL_REL, errs
+
+
+def test_tiny_fp32_tf32_path():
+    x = make_inputs("tiny")
+    g = _gpu_run(x)
+    ref = oracle.forward_backward(x.H.astype(np.float64), x.W.astype(np.float64), x.targets, IGNORE_INDEX)
+    valid = x.targets != IGNORE_INDEX
+    errs = {"loss": abs(g["loss"] - ref["loss"]),
+            "lse": float(np.max(np.abs(g["lse"][valid] - ref["lse"]))),
+            "dH": rel_fro(np64(g["dH"]), ref["dH"]), "dW": rel_fro(np64(g["dW"]), ref["dW"])}
+    print("tiny fp32", errs)
+    assert errs["loss"] <= 2e-3 and errs["lse"] <= 5e-3, errs
+    assert errs["dH"] <= 1e-2 and errs["dW"] <= 1e-2, errs
+
+
+def test_peak_memory_is_not_n_times_v():
+    """Extra device memory of one call on the largest-vocab workload stays far
+    below the N x V fp32 logits it avoids (17.2 GB here)."""
+    x = make_inputs("vocab256k")
+    H, W, t = to_device(x)
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats()
+    base = torch.cuda.memory_allocated()
+    w = x.workload
+    ws = torch.empty(lce.workspace_size(w.N, w.d, w.V), dtype=torch.uint8, device="cuda")
+    loss, dH, dW = lce.lce_forward_backward(H, W, t, IGNORE_INDEX, workspace=ws)
+    torch.cuda.synchronize()
+    extra = torch.cuda.max_memory_allocated() - base - dH.numel() * 2 - dW.numel() * 4 - 512
+    logits = w.N * w.V * 4
+    print("extra bytes", extra, "logits bytes", logits)
+    assert extra <= logits / 10
