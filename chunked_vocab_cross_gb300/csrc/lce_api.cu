@@ -112,12 +112,8 @@ lce_status_t device_info(DevInfo **out) {
         di.major = p.major;
         di.minor = p.minor;
         if (!(di.major == 10 && di.minor == 3) || di.sms > kMaxSms) return LCE_ERR_DEVICE;
-        const void *gemms[] = {
-            (const void *)k_gemm<__nv_bfloat16, MODE_LSE>, (const void *)k_gemm<__nv_bfloat16, MODE_G>,
-            (const void *)k_gemm<__nv_bfloat16, MODE_DH>,  (const void *)k_gemm<__nv_bfloat16, MODE_DW>,
-            (const void *)k_gemm<float, MODE_LSE>,         (const void *)k_gemm<float, MODE_G>,
-            (const void *)k_gemm<float, MODE_DH>,          (const void *)k_gemm<float, MODE_DW>,
-        };
+        const void *gemms[] = {(const void *)k_gemm<MODE_LSE>, (const void *)k_gemm<MODE_G>,
+                               (const void *)k_gemm<MODE_DH>, (const void *)k_gemm<MODE_DW>};
         for (const void *f : gemms) {
             e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
             if (e != cudaSuccess) {
@@ -141,16 +137,15 @@ lce_status_t device_info(DevInfo **out) {
     return LCE_OK;
 }
 
-bool encode_map(CUtensorMap *m, lce_dtype_t dt, const void *base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+// 2-D bf16 tensor map over a row-major [outer][inner] array, 128-byte swizzle.
+bool encode_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_inner,
                 uint32_t box_outer) {
-    const uint64_t elt = dt == LCE_BF16 ? 2 : 4;
     cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * elt};
+    cuuint64_t strides[1] = {inner * 2};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t es[2] = {1, 1};
-    CUresult r = g_encode(m, dt == LCE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-                          const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -161,13 +156,16 @@ inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
     int64_t N_pad = 0, Vc = 0, part_rows = 0;
-    size_t idx = 0, inv = 0, counters = 0, tc = 0, z = 0, lse2 = 0, loss_rows = 0, part = 0, Hc = 0, G = 0,
-           dHacc = 0, total = 0;
+    size_t idx = 0, inv = 0, counters = 0, tc = 0, z = 0, lse2 = 0, loss_rows = 0, part = 0, Hc = 0, Hc_lo = 0,
+           W_hi = 0, W_lo = 0, G = 0, G_lo = 0, dHacc = 0, total = 0;
 };
 
+// Every operand the tensor cores read is bf16. fp32 inputs are carried as bf16
+// hi/lo pairs (Hc/Hc_lo, W_hi/W_lo, G/G_lo), so the fp32 path also holds a
+// split copy of W (4*V*d bytes).
 Layout make_layout(int64_t N, int64_t d, int64_t V, lce_dtype_t dt, int64_t Vc, bool backward) {
     Layout L;
-    const size_t elt = dt == LCE_BF16 ? 2 : 4;
+    const bool split = dt == LCE_FP32;
     L.N_pad = (N + kBM - 1) / kBM * kBM;
     L.Vc = Vc;
     L.part_rows = lse_partial_rows(static_cast<int>(L.N_pad), kMaxSms);
@@ -185,9 +183,15 @@ Layout make_layout(int64_t N, int64_t d, int64_t V, lce_dtype_t dt, int64_t Vc, 
     L.lse2 = take(L.N_pad * 4);
     L.loss_rows = take(L.N_pad * 4);
     L.part = take(L.part_rows * 8);
-    L.Hc = take(L.N_pad * d * elt);
+    L.Hc = take(L.N_pad * d * 2);
+    if (split) {
+        L.Hc_lo = take(L.N_pad * d * 2);
+        L.W_hi = take(static_cast<size_t>(V) * d * 2);
+        L.W_lo = take(static_cast<size_t>(V) * d * 2);
+    }
     if (backward) {
-        L.G = take(L.N_pad * Vc * elt);
+        L.G = take(L.N_pad * Vc * 2);
+        if (split) L.G_lo = take(L.N_pad * Vc * 2);
         L.dHacc = take(L.N_pad * d * 4);
     }
     L.total = o;
@@ -211,8 +215,7 @@ lce_status_t check_args(const lce_args_t *a) {
     if (a->vocab_chunk < 0 || (a->vocab_chunk > 0 && (a->vocab_chunk % kBN) != 0) ||
         a->vocab_chunk > (int64_t(1) << 20))
         return LCE_ERR_SHAPE;
-    const int64_t elt = a->dtype == LCE_BF16 ? 2 : 4;
-    if ((a->d * elt) % 16) return LCE_ERR_ALIGN;
+    if (a->d % 8) return LCE_ERR_ALIGN;   // bf16 rows (operands or their split copies) of 16-byte multiples
     auto mis = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
     if (mis(a->H) || mis(a->W) || (a->dH && mis(a->dH)) || (a->dW && mis(a->dW)) ||
         (a->workspace && mis(a->workspace)))
@@ -243,6 +246,7 @@ template <typename T>
 lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(a->stream);
     const bool backward = a->dH != nullptr;
+    const bool split = a->dtype == LCE_FP32;
     const int64_t Vc = pick_chunk(a->V, a->vocab_chunk);
     const Layout L = make_layout(a->N, a->d, a->V, a->dtype, Vc, backward);
     const int N = static_cast<int>(a->N), d = static_cast<int>(a->d), V = static_cast<int>(a->V);
@@ -261,6 +265,7 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
         ws.owned = true;
     }
     uint8_t *base = static_cast<uint8_t *>(ws.p);
+    auto bf = [&](size_t off) { return reinterpret_cast<__nv_bfloat16 *>(base + off); };
     int *idx = reinterpret_cast<int *>(base + L.idx);
     int *inv = reinterpret_cast<int *>(base + L.inv);
     int *counters = reinterpret_cast<int *>(base + L.counters);
@@ -269,15 +274,19 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
     float *lse2 = reinterpret_cast<float *>(base + L.lse2);
     float *loss_rows = reinterpret_cast<float *>(base + L.loss_rows);
     float2 *part = reinterpret_cast<float2 *>(base + L.part);
-    T *Hc = reinterpret_cast<T *>(base + L.Hc);
-    T *G = backward ? reinterpret_cast<T *>(base + L.G) : nullptr;
+    __nv_bfloat16 *Hc = bf(L.Hc);
+    __nv_bfloat16 *Hc_lo = split ? bf(L.Hc_lo) : nullptr;
+    const __nv_bfloat16 *W_hi = split ? bf(L.W_hi) : static_cast<const __nv_bfloat16 *>(a->W);
+    const __nv_bfloat16 *W_lo = split ? bf(L.W_lo) : W_hi;
+    __nv_bfloat16 *G = backward ? bf(L.G) : nullptr;
+    __nv_bfloat16 *G_lo = backward && split ? bf(L.G_lo) : G;
     float *dHacc = backward ? reinterpret_cast<float *>(base + L.dHacc) : nullptr;
+    const __nv_bfloat16 *Hc_lo_or_hi = split ? Hc_lo : Hc;
 
-    const int bk = Tile<T>::kBK;
-    const int atom = Tile<T>::kAtom;
-    CUtensorMap tmHc_k, tmW_k;
-    if (!encode_map(&tmHc_k, a->dtype, Hc, d, L.N_pad, bk, kBM) ||
-        !encode_map(&tmW_k, a->dtype, a->W, d, V, bk, kBN))
+    // K-major operand maps (box 64 x rows) and MN-major ones (box 64 x 64)
+    CUtensorMap tmHc_k, tmHcl_k, tmW_k, tmWl_k;
+    if (!encode_map(&tmHc_k, Hc, d, L.N_pad, kBK, kBM) || !encode_map(&tmHcl_k, Hc_lo_or_hi, d, L.N_pad, kBK, kBM) ||
+        !encode_map(&tmW_k, W_hi, d, V, kBK, kBN) || !encode_map(&tmWl_k, W_lo, d, V, kBK, kBN))
         return LCE_ERR_CUDA;
 
     GemmArgs ga{};
@@ -285,6 +294,7 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
     ga.d = d;
     ga.V = V;
     ga.num_sms = di.sms;
+    ga.nseg = split ? 3 : 1;
     ga.tc = tc;
     ga.grad_scale = a->grad_scale == 0.f ? 1.f : a->grad_scale;
     const int n_tiles_v = cdiv(V, kBN);
@@ -294,9 +304,14 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
         k_compact<<<1, kCompactThreads, 0, st>>>(a->targets, N, a->ignore_index, a->V, idx, inv, counters, a->lse);
         LCE_CHECK_LAUNCH();
         const int grid = static_cast<int>(L.N_pad < 4 * di.sms * 8 ? L.N_pad : 4 * di.sms * 8);
-        k_gather<T><<<grid, 256, 0, st>>>(static_cast<const T *>(a->H), a->targets, d, a->V, idx, counters, Hc, tc,
-                                           z);
+        k_gather<T><<<grid, 256, 0, st>>>(static_cast<const T *>(a->H), a->targets, d, a->V, idx, counters, Hc,
+                                           Hc_lo, tc, z);
         LCE_CHECK_LAUNCH();
+        if (split) {
+            k_split_rows<<<4 * di.sms, 256, 0, st>>>(static_cast<const float *>(a->W), static_cast<size_t>(V) * d,
+                                                     bf(L.W_hi), bf(L.W_lo));
+            LCE_CHECK_LAUNCH();
+        }
     }
     {
         PhaseScope ph(1, st);
@@ -305,7 +320,7 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
         g.vlen = V;
         g.z = z;
         g.part = part;
-        k_gemm<T, MODE_LSE><<<di.sms, kThreads, kGemmSmem, st>>>(tmHc_k, tmW_k, g);
+        k_gemm<MODE_LSE><<<di.sms, kThreads, kGemmSmem, st>>>(tmHc_k, tmHcl_k, tmW_k, tmWl_k, g);
         LCE_CHECK_LAUNCH();
     }
     {
@@ -318,14 +333,14 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
     }
     if (!backward) return LCE_OK;
 
-    CUtensorMap tmG_k, tmG_mn, tmHc_mn, tmW_mn;
-    if (!encode_map(&tmG_k, a->dtype, G, Vc, L.N_pad, bk, kBM) ||
-        !encode_map(&tmG_mn, a->dtype, G, Vc, L.N_pad, atom, bk) ||
-        !encode_map(&tmHc_mn, a->dtype, Hc, d, L.N_pad, atom, bk) ||
-        !encode_map(&tmW_mn, a->dtype, a->W, d, V, atom, bk))
+    CUtensorMap tmG_k, tmGl_k, tmG_mn, tmGl_mn, tmHc_mn, tmHcl_mn, tmW_mn, tmWl_mn;
+    if (!encode_map(&tmG_k, G, Vc, L.N_pad, kBK, kBM) || !encode_map(&tmGl_k, G_lo, Vc, L.N_pad, kBK, kBM) ||
+        !encode_map(&tmG_mn, G, Vc, L.N_pad, kAtom, kBK) || !encode_map(&tmGl_mn, G_lo, Vc, L.N_pad, kAtom, kBK) ||
+        !encode_map(&tmHc_mn, Hc, d, L.N_pad, kAtom, kBK) ||
+        !encode_map(&tmHcl_mn, Hc_lo_or_hi, d, L.N_pad, kAtom, kBK) ||
+        !encode_map(&tmW_mn, W_hi, d, V, kAtom, kBK) || !encode_map(&tmWl_mn, W_lo, d, V, kAtom, kBK))
         return LCE_ERR_CUDA;
 
-    const int dw_grid_cap = di.sms;
     for (int64_t v0 = 0; v0 < a->V; v0 += Vc) {
         const int vlen = static_cast<int>(a->V - v0 < Vc ? a->V - v0 : Vc);
         GemmArgs g = ga;
@@ -333,10 +348,11 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
         g.vlen = vlen;
         g.ldg = static_cast<int>(Vc);
         g.G = G;
+        g.G_lo = G_lo;
         g.lse2 = lse2;
         {
             PhaseScope ph(3, st);
-            k_gemm<T, MODE_G><<<di.sms, kThreads, kGemmSmem, st>>>(tmHc_k, tmW_k, g);
+            k_gemm<MODE_G><<<di.sms, kThreads, kGemmSmem, st>>>(tmHc_k, tmHcl_k, tmW_k, tmWl_k, g);
             LCE_CHECK_LAUNCH();
         }
         {
@@ -345,8 +361,8 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
             gw.dW = a->dW;
             gw.accumulate = a->accumulate_dW ? 1 : 0;
             const int units = cdiv(vlen, kBM) * cdiv(d, kBN);
-            k_gemm<T, MODE_DW><<<units < dw_grid_cap ? units : dw_grid_cap, kThreads, kGemmSmem, st>>>(tmG_mn,
-                                                                                                      tmHc_mn, gw);
+            k_gemm<MODE_DW><<<units < di.sms ? units : di.sms, kThreads, kGemmSmem, st>>>(tmG_mn, tmGl_mn, tmHc_mn,
+                                                                                        tmHcl_mn, gw);
             LCE_CHECK_LAUNCH();
         }
         {
@@ -354,7 +370,7 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
             GemmArgs gh = g;
             gh.dH_acc = dHacc;
             gh.accumulate = v0 > 0 ? 1 : 0;
-            k_gemm<T, MODE_DH><<<di.sms, kThreads, kGemmSmem, st>>>(tmG_k, tmW_mn, gh);
+            k_gemm<MODE_DH><<<di.sms, kThreads, kGemmSmem, st>>>(tmG_k, tmGl_k, tmW_mn, tmWl_mn, gh);
             LCE_CHECK_LAUNCH();
         }
     }

@@ -5,22 +5,29 @@
 //   warp 0      TMA producer: streams A and B k-blocks into a 4-stage
 //               shared-memory ring (128-byte swizzle), signalling mbarriers.
 //   warp 1      owns TMEM (512 columns = two 128x256 fp32 accumulators) and
-//               issues tcgen05.mma 128x256xK from one thread.
+//               issues tcgen05.mma.kind::f16 128x256x16 (bf16 in, fp32
+//               accumulate) from one thread.
 //   warps 2..5  epilogue: tcgen05.ld the finished accumulator (warp w reads
 //               TMEM lanes 32*(w%4)..+31, one tile row per thread) while the
 //               MMA thread already fills the other accumulator.
 //
-// Modes (A x B^T, all operands bf16 or tf32 in shared memory, fp32 in TMEM):
+// Modes (D = A . B^T in TMEM):
 //   MODE_LSE  S = Hc . W^T      per 128-row block over a contiguous range of
 //             256-wide vocab tiles; the epilogue carries the online
 //             (max, sum) of exp over the row in registers and writes one
 //             (m, l) partial per row and range, plus the target logit.
 //   MODE_G    S = Hc . W_c^T    over one vocab chunk; the epilogue forms
-//             G = (exp(S - lse) - onehot) * scale / Nv and stores it.
+//             G = (exp(S - lse) - onehot) * scale / Nv and stores it (bf16).
 //   MODE_DW   dW_c = G^T . Hc   (M = chunk vocab rows, K = valid tokens);
 //             A and B are read MN-major straight from G and Hc.
-//   MODE_DH   dHacc += G . W_c  (M = valid tokens, K = chunk vocab rows);
+//   MODE_DH   dHacc (+)= G . W_c (M = valid tokens, K = chunk vocab rows);
 //             B is read MN-major straight from W.
+//
+// Split precision (fp32 inputs): every fp32 operand x is carried as two bf16
+// tensors, x = hi + lo with hi = bf16(x) and lo = bf16(x - hi), and the K loop
+// runs three segments, A_hi.B_hi + A_hi.B_lo + A_lo.B_hi, into the same
+// accumulator (the lo.lo term is below fp32 resolution of the sum). With
+// nseg = 1 only the hi tensors are read.
 //
 // Every wait is bounded: on time-out the CTA raises LCE_DEV_TIMEOUT in the
 // device status word, lets its in-flight copies and MMAs land, frees TMEM and
@@ -36,6 +43,10 @@ namespace lce {
 
 constexpr int kBM = 128;          // tile rows   (UMMA M)
 constexpr int kBN = 256;          // tile cols   (UMMA N)
+constexpr int kBK = 64;           // k per stage: one 128-byte bf16 line
+constexpr int kUmmaK = 16;        // k per tcgen05.mma (bf16)
+constexpr int kAtom = 64;         // MN elements per 128-byte line
+constexpr int kAtomBytes = kBK * 128;   // one MN-major box {64 (MN), 64 (K)} = 8 KB
 constexpr int kStages = 4;
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;    // two 256-column fp32 accumulators
@@ -46,6 +57,7 @@ constexpr int kGemmSmem = kStages * kStageBytes + 1024 /*alignment slack*/ + 256
 constexpr long long kWaitCycles = 2000000000LL;   // ~1 s: far above any legitimate wait
 constexpr long long kDrainCycles = 200000000LL;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kFmtBf16 = 1u;   // operand format code of bf16 in the f16-kind descriptor
 
 enum GemmMode : int { MODE_LSE = 0, MODE_G = 1, MODE_DH = 2, MODE_DW = 3 };
 enum DevStatus : int { DEV_TARGET_RANGE = 1, DEV_TIMEOUT = 2 };
@@ -53,26 +65,6 @@ enum DevStatus : int { DEV_TARGET_RANGE = 1, DEV_TIMEOUT = 2 };
 // Device status word (LCE_DEV_* bits). The library is one translation unit,
 // so this header is the single definition.
 __device__ int g_status = 0;
-
-template <typename T>
-struct Elem;
-template <>
-struct Elem<__nv_bfloat16> {
-    static constexpr uint32_t kFmt = 1;   // bf16
-};
-template <>
-struct Elem<float> {
-    static constexpr uint32_t kFmt = 2;   // tf32
-};
-
-template <typename T>
-struct Tile {
-    static constexpr int kBytes = sizeof(T);
-    static constexpr int kBK = 128 / kBytes;        // k per stage: one 128-byte line
-    static constexpr int kUmmaK = 32 / kBytes;      // k per tcgen05.mma
-    static constexpr int kAtom = 128 / kBytes;      // MN elements per 128-byte line
-    static constexpr int kAtomBytes = kBK * 128;    // one MN-major box {kAtom, kBK}
-};
 
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
@@ -109,12 +101,14 @@ struct GemmArgs {
     int v0;                // first vocab row of the chunk (0 for MODE_LSE)
     int vlen;              // vocab rows in the chunk (V for MODE_LSE)
     int num_sms;
+    int nseg;              // 1 (bf16 operands) or 3 (split-precision fp32 operands)
     int ldg;               // row stride of G in elements
     const int *tc;         // compacted targets, -1 where none
     const float *lse2;     // per compacted row: lse / ln 2   (MODE_G)
     float *z;              // per compacted row: target logit (MODE_LSE)
     float2 *part;          // (m, l) partials [splits][m_blocks*128] (MODE_LSE)
-    void *G;               // G chunk [rows][ldg]            (MODE_G)
+    __nv_bfloat16 *G;      // G chunk [rows][ldg], hi part     (MODE_G)
+    __nv_bfloat16 *G_lo;   // lo part when nseg == 3           (MODE_G)
     float *dW;             // [V][d]                           (MODE_DW)
     float *dH_acc;         // [rows][d]                        (MODE_DH)
     int accumulate;        // DW / DH: add into the output instead of overwriting
@@ -122,27 +116,27 @@ struct GemmArgs {
 };
 
 struct Sched {
-    int m_blocks, n_tiles, k_blocks, splits, units;
+    int m_blocks, n_tiles, k_seg, k_blocks, splits, units;
 };
 
-template <typename T, int MODE>
+template <int MODE>
 __device__ inline Sched make_sched(const GemmArgs &a, int nv) {
     Sched s;
-    const int bk = Tile<T>::kBK;
     s.splits = 1;
     if (MODE == MODE_LSE || MODE == MODE_G) {
         s.m_blocks = cdiv(nv, kBM);
         s.n_tiles = cdiv(a.vlen, kBN);
-        s.k_blocks = cdiv(a.d, bk);
+        s.k_seg = cdiv(a.d, kBK);
     } else if (MODE == MODE_DH) {
         s.m_blocks = cdiv(nv, kBM);
         s.n_tiles = cdiv(a.d, kBN);
-        s.k_blocks = cdiv(a.vlen, bk);
+        s.k_seg = cdiv(a.vlen, kBK);
     } else {
         s.m_blocks = cdiv(a.vlen, kBM);
         s.n_tiles = cdiv(a.d, kBN);
-        s.k_blocks = cdiv(nv, bk);
+        s.k_seg = cdiv(nv, kBK);
     }
+    s.k_blocks = s.k_seg * a.nseg;
     if (MODE == MODE_LSE) {
         s.splits = lse_splits(s.m_blocks, s.n_tiles, a.num_sms);
         s.units = s.m_blocks * s.splits;
@@ -205,13 +199,30 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-template <typename T, int MODE>
+// fp32 -> (hi, lo) with hi = bf16(x) and lo = x - hi (exact in fp32; the
+// caller rounds lo to bf16 when it stores it).
+__device__ __forceinline__ void split_bf16(float x, float &hi, float &lo) {
+    const float h = __bfloat162float(__float2bfloat16_rn(x));
+    lo = x - h;
+    hi = h;
+}
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const float (&g)[32]) {
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        d4[q] = make_uint4(pack_bf16x2(g[8 * q + 0], g[8 * q + 1]), pack_bf16x2(g[8 * q + 2], g[8 * q + 3]),
+                           pack_bf16x2(g[8 * q + 4], g[8 * q + 5]), pack_bf16x2(g[8 * q + 6], g[8 * q + 7]));
+}
+
+// tmA0/tmB0 hold the bf16 (hi) operands; tmA1/tmB1 the lo parts (nseg == 3).
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
-    using TT = Tile<T>;
+    k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+           const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1, const GemmArgs a) {
     constexpr bool kAmn = (MODE == MODE_DW);
     constexpr bool kBmn = (MODE == MODE_DH || MODE == MODE_DW);
-    constexpr uint32_t kIdesc = idesc_f32acc(Elem<T>::kFmt, kBM, kBN, kAmn, kBmn);
+    constexpr uint32_t kIdesc = idesc_f32acc(kFmtBf16, kBM, kBN, kAmn, kBmn);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -226,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int nv = a.counters[0];
-    const Sched s = make_sched<T, MODE>(a, nv);
+    const Sched s = make_sched<MODE>(a, nv);
     if (static_cast<int>(blockIdx.x) >= s.units) return;   // uniform over the CTA
 
     if (threadIdx.x == 0) {
@@ -243,8 +254,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
-        tma_prefetch_map(&tmA);
-        tma_prefetch_map(&tmB);
+        tma_prefetch_map(&tmA0);
+        tma_prefetch_map(&tmB0);
+        if (a.nseg > 1) {
+            tma_prefetch_map(&tmA1);
+            tma_prefetch_map(&tmB1);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
@@ -264,32 +279,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int mb, n0, n1, sp;
                 unit_tiles<MODE>(s, u, mb, n0, n1, sp);
                 for (int nt = n0; ok && nt < n1; ++nt) {
-                    for (int kb = 0; kb < s.k_blocks; ++kb, ++it) {
+                    for (int kbt = 0; kbt < s.k_blocks; ++kbt, ++it) {
                         const int st = it % kStages;
                         if (!wait_bar(&empty[st], ((it / kStages) & 1) ^ 1, abort_flag)) {
                             ok = false;
                             break;
                         }
+                        // segment 0: hi.hi, 1: hi.lo, 2: lo.hi
+                        const int seg = kbt / s.k_seg;
+                        const int kb = kbt - seg * s.k_seg;
+                        const CUtensorMap *ma = seg == 2 ? &tmA1 : &tmA0;
+                        const CUtensorMap *mbp = seg == 1 ? &tmB1 : &tmB0;
                         mbar_arrive_expect_tx(&full[st], kStageBytes);
                         uint8_t *sa = smem + st * kStageBytes;
                         uint8_t *sb = sa + kStageA;
-                        const int k0 = kb * TT::kBK;
+                        const int k0 = kb * kBK;
                         if (MODE == MODE_LSE || MODE == MODE_G) {
-                            tma_load_2d(sa, &tmA, &full[st], k0, mb * kBM);
-                            tma_load_2d(sb, &tmB, &full[st], k0, a.v0 + nt * kBN);
+                            tma_load_2d(sa, ma, &full[st], k0, mb * kBM);
+                            tma_load_2d(sb, mbp, &full[st], k0, a.v0 + nt * kBN);
                         } else if (MODE == MODE_DH) {
-                            tma_load_2d(sa, &tmA, &full[st], k0, mb * kBM);
+                            tma_load_2d(sa, ma, &full[st], k0, mb * kBM);
 #pragma unroll
-                            for (int b = 0; b < kBN / TT::kAtom; ++b)
-                                tma_load_2d(sb + b * TT::kAtomBytes, &tmB, &full[st], nt * kBN + b * TT::kAtom,
-                                            a.v0 + k0);
+                            for (int b = 0; b < kBN / kAtom; ++b)
+                                tma_load_2d(sb + b * kAtomBytes, mbp, &full[st], nt * kBN + b * kAtom, a.v0 + k0);
                         } else {
 #pragma unroll
-                            for (int b = 0; b < kBM / TT::kAtom; ++b)
-                                tma_load_2d(sa + b * TT::kAtomBytes, &tmA, &full[st], mb * kBM + b * TT::kAtom, k0);
+                            for (int b = 0; b < kBM / kAtom; ++b)
+                                tma_load_2d(sa + b * kAtomBytes, ma, &full[st], mb * kBM + b * kAtom, k0);
 #pragma unroll
-                            for (int b = 0; b < kBN / TT::kAtom; ++b)
-                                tma_load_2d(sb + b * TT::kAtomBytes, &tmB, &full[st], nt * kBN + b * TT::kAtom, k0);
+                            for (int b = 0; b < kBN / kAtom; ++b)
+                                tma_load_2d(sb + b * kAtomBytes, mbp, &full[st], nt * kBN + b * kAtom, k0);
                         }
                     }
                 }
@@ -326,15 +345,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t sa = smem_u32(smem + st * kStageBytes);
                         const uint32_t sb = sa + kStageA;
 #pragma unroll
-                        for (int kk = 0; kk < TT::kBK / TT::kUmmaK; ++kk) {
-                            const uint64_t ad = kAmn ? sdesc_sw128(sa + kk * TT::kUmmaK * 128, TT::kAtomBytes, 1024)
+                        for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+                            const uint64_t ad = kAmn ? sdesc_sw128(sa + kk * kUmmaK * 128, kAtomBytes, 1024)
                                                      : sdesc_sw128(sa + kk * 32, 16, 1024);
-                            const uint64_t bd = kBmn ? sdesc_sw128(sb + kk * TT::kUmmaK * 128, TT::kAtomBytes, 1024)
+                            const uint64_t bd = kBmn ? sdesc_sw128(sb + kk * kUmmaK * 128, kAtomBytes, 1024)
                                                      : sdesc_sw128(sb + kk * 32, 16, 1024);
-                            if (sizeof(T) == 2)
-                                umma_f16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0);
-                            else
-                                umma_tf32(d_tmem, ad, bd, kIdesc, (kb | kk) != 0);
+                            umma_f16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0);
                         }
                         umma_commit(&empty[st]);   // frees the stage once these MMAs have read it
                     }
@@ -356,10 +372,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             int mb, n0, n1, sp;
             unit_tiles<MODE>(s, u, mb, n0, n1, sp);
             const int grow = mb * kBM + trow;      // compacted row (LSE/G/DH) or chunk vocab row (DW)
+            // target column relative to the first column this launch covers (the
+            // chunk start v0 in MODE_G), negative / out of range when absent
             int tgt = -1;
             float lse2 = 0.f;
-            // target column relative to the first column this launch covers (the
-            // chunk start v0 in MODE_G), -1 / out of range when absent
             if (MODE == MODE_LSE || MODE == MODE_G) tgt = grow < nv ? a.tc[grow] - a.v0 : -1;
             if (MODE == MODE_G) lse2 = grow < nv ? a.lse2[grow] : INFINITY;
             float run_m = -INFINITY, run_l = 0.f;
@@ -402,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             run_m = mn;
                         }
                     } else if (MODE == MODE_G) {
-                        T *gp = reinterpret_cast<T *>(a.G) + static_cast<size_t>(grow) * a.ldg + col;
+                        const size_t off = static_cast<size_t>(grow) * a.ldg + col;
                         float g[32];
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
@@ -410,19 +426,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (col + j == tgt) v -= inv_nv;
                             g[j] = (col + j < a.vlen) ? v : 0.f;
                         }
-                        if (sizeof(T) == 2) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(gp);
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                dst[q] = make_uint4(pack_bf16x2(g[8 * q + 0], g[8 * q + 1]),
-                                                    pack_bf16x2(g[8 * q + 2], g[8 * q + 3]),
-                                                    pack_bf16x2(g[8 * q + 4], g[8 * q + 5]),
-                                                    pack_bf16x2(g[8 * q + 6], g[8 * q + 7]));
+                        if (a.nseg == 1) {
+                            store_bf16x32(a.G + off, g);
                         } else {
-                            float4 *dst = reinterpret_cast<float4 *>(gp);
+                            float lo[32];
 #pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                dst[q] = make_float4(g[4 * q], g[4 * q + 1], g[4 * q + 2], g[4 * q + 3]);
+                            for (int j = 0; j < 32; ++j) split_bf16(g[j], g[j], lo[j]);
+                            store_bf16x32(a.G + off, g);
+                            store_bf16x32(a.G_lo + off, lo);
                         }
                     } else {
                         // DW: row = chunk vocab row, out = dW[v0 + row]; DH: row = compacted token

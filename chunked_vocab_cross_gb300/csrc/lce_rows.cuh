@@ -70,26 +70,59 @@ __global__ void __launch_bounds__(kCompactThreads)
 
 // Hc[r] = H[idx[r]] for r < Nv, zero rows on [Nv, round_up(Nv, 128)) so the
 // tensor-core passes can read whole 128-row blocks; tc[r] = target (or -1),
-// z[r] = NaN until the logits pass finds the target column.
+// z[r] = NaN until the logits pass finds the target column. bf16 rows are
+// copied; fp32 rows are split into bf16 hi and lo parts (Hc, Hc_lo).
+__device__ __forceinline__ void gather8(const __nv_bfloat16 *src, __nv_bfloat16 *hi, __nv_bfloat16 *, bool live) {
+    *reinterpret_cast<uint4 *>(hi) = live ? *reinterpret_cast<const uint4 *>(src) : make_uint4(0, 0, 0, 0);
+}
+__device__ __forceinline__ void gather8(const float *src, __nv_bfloat16 *hi, __nv_bfloat16 *lo, bool live) {
+    float h[8], l[8];
+    if (live) {
+        const float4 a = reinterpret_cast<const float4 *>(src)[0];
+        const float4 b = reinterpret_cast<const float4 *>(src)[1];
+        const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) split_bf16(x[j], h[j], l[j]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) h[j] = l[j] = 0.f;
+    }
+    *reinterpret_cast<uint4 *>(hi) =
+        make_uint4(pack_bf16x2(h[0], h[1]), pack_bf16x2(h[2], h[3]), pack_bf16x2(h[4], h[5]), pack_bf16x2(h[6], h[7]));
+    *reinterpret_cast<uint4 *>(lo) =
+        make_uint4(pack_bf16x2(l[0], l[1]), pack_bf16x2(l[2], l[3]), pack_bf16x2(l[4], l[5]), pack_bf16x2(l[6], l[7]));
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256)
     k_gather(const T *__restrict__ H, const int64_t *__restrict__ t, int d, int64_t V, const int *__restrict__ idx,
-             const int *__restrict__ counters, T *__restrict__ Hc, int *__restrict__ tc, float *__restrict__ z) {
+             const int *__restrict__ counters, __nv_bfloat16 *__restrict__ Hc, __nv_bfloat16 *__restrict__ Hc_lo,
+             int *__restrict__ tc, float *__restrict__ z) {
     const int nv = counters[0];
     const int rows = cdiv(nv, kBM) * kBM;
-    const int vec = d * static_cast<int>(sizeof(T)) / 16;
+    const int groups = d / 8;   // d is a multiple of 8
     for (int r = blockIdx.x; r < rows; r += gridDim.x) {
         const bool live = r < nv;
         const int src_row = live ? idx[r] : 0;
-        const uint4 *src = reinterpret_cast<const uint4 *>(H + static_cast<size_t>(src_row) * d);
-        uint4 *dst = reinterpret_cast<uint4 *>(Hc + static_cast<size_t>(r) * d);
-        for (int c = threadIdx.x; c < vec; c += blockDim.x) dst[c] = live ? src[c] : make_uint4(0, 0, 0, 0);
+        const T *src = H + static_cast<size_t>(src_row) * d;
+        __nv_bfloat16 *hi = Hc + static_cast<size_t>(r) * d;
+        __nv_bfloat16 *lo = Hc_lo ? Hc_lo + static_cast<size_t>(r) * d : nullptr;
+        for (int g = threadIdx.x; g < groups; g += blockDim.x) gather8(src + 8 * g, hi + 8 * g, lo ? lo + 8 * g : nullptr, live);
         if (threadIdx.x == 0) {
             const int64_t tt = live ? t[src_row] : -1;
             tc[r] = (tt >= 0 && tt < V) ? static_cast<int>(tt) : -1;
             z[r] = __int_as_float(0x7fc00000);
         }
     }
+}
+
+// W (fp32) -> W_hi, W_lo (bf16) for the split-precision path; n % 8 == 0.
+__global__ void __launch_bounds__(256)
+    k_split_rows(const float *__restrict__ W, size_t n, __nv_bfloat16 *__restrict__ hi, __nv_bfloat16 *__restrict__ lo) {
+    const size_t groups = n / 8;
+    for (size_t g = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; g < groups;
+         g += static_cast<size_t>(gridDim.x) * blockDim.x)
+        gather8(W + 8 * g, hi + 8 * g, lo + 8 * g, true);
 }
 
 // Merge the per-range (m, l) partials of each row (log2 units) in fixed range

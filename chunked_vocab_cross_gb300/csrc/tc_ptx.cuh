@@ -94,17 +94,6 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
-// Same with tf32 inputs (fp32 storage, tensor cores read the tf32 part).
-__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                          uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // Arrive once on `bar` when every UMMA this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -154,10 +143,9 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
-// Instruction descriptor for kind::f16 / kind::tf32 with an fp32 accumulator.
-//   bits 4-5 D format (1 = f32); 7-9 A format, 10-12 B format (1 = bf16,
-//   2 = tf32); bit 15 A is MN-major; bit 16 B is MN-major; 17-22 N >> 3;
-//   24-28 M >> 4.
+// Instruction descriptor for kind::f16 with an fp32 accumulator.
+//   bits 4-5 D format (1 = f32); 7-9 A format, 10-12 B format (1 = bf16);
+//   bit 15 A is MN-major; bit 16 B is MN-major; 17-22 N >> 3; 24-28 M >> 4.
 __host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t fmt, int M, int N, bool a_mn, bool b_mn) {
     return (1u << 4) | (fmt << 7) | (fmt << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);

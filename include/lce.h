@@ -27,9 +27,14 @@
  *    and contiguous; the library never frees or retains them after the call.
  *  - H, W (and dH) are bf16 for lce_forward / lce_forward_backward, or the
  *    dtype given in lce_args_t; dW, loss and lse are fp32.
- *  - H, W, dH, dW base pointers must be 16-byte aligned and d*sizeof(elem)
- *    a multiple of 16 (d % 8 == 0 for bf16, d % 4 == 0 for fp32): W and the
- *    compacted H are read by the Tensor Memory Accelerator.
+ *  - H, W, dH, dW base pointers must be 16-byte aligned and d % 8 == 0:
+ *    W and the compacted H are read by the Tensor Memory Accelerator in rows
+ *    of 16-byte multiples.
+ *  - bf16 inputs run on bf16 tensor cores with fp32 accumulation. fp32
+ *    inputs are split into bf16 pairs x = hi + lo and every product is formed
+ *    as hi.hi + hi.lo + lo.hi (three times the tensor work, relative error
+ *    about 2^-16); that path also holds a bf16 split copy of W (4*V*d bytes)
+ *    in its workspace.
  *  - 1 <= N < 2^31, 1 <= d <= 65536, 1 <= V < 2^31.
  *  - Work is enqueued on `stream` (NULL = the legacy default stream) and the
  *    call returns without synchronising. Scratch memory is stream-ordered

@@ -105,6 +105,19 @@ def test_small_bf16_parity(shape):
     _run_and_compare(x)
 
 
+FP32 = [(1, 64, 1000), (300, 128, 1000), (700, 200, 4099), (333, 64, 300)]
+
+
+@pytest.mark.parametrize("shape", FP32, ids=lambda s: f"N{s[0]}_d{s[1]}_V{s[2]}")
+def test_small_fp32_split_parity(shape):
+    """fp32 inputs through the split-precision (bf16 hi/lo) tensor-core path,
+    including several vocab chunks."""
+    N, d, V = shape
+    x = make_inputs("tiny", N=N, d=d, V=V, padding=("random_frac", 0.1))
+    errs = _run_and_compare(x, vocab_chunk=1024)
+    assert errs["loss"] <= 1e-4 and errs["dH"] <= 1e-3 and errs["dW"] <= 1e-3, errs
+
+
 @pytest.mark.parametrize("vocab_chunk", [256, 768, 1024])
 def test_vocab_chunk_sizes(vocab_chunk):
     x = make_inputs("gpt1b", N=500, d=256, V=2900, padding=("random_frac", 0.2), seqs=1)

@@ -6,9 +6,9 @@ benchmark times (lce_run with a caller workspace):
   llama8b     full loss and every row's lse; dH on 256 seeded token rows and
               dW on 256 seeded vocab rows
   vocab256k   same sampling as llama8b
-Tolerances: bf16 inputs |loss| <= 1e-3, relative Frobenius <= 5e-3 for dH and
-dW, per-row lse <= 1e-3 (diagnostic). fp32 inputs run on tf32 tensor cores
-(10 explicit mantissa bits): |loss| <= 2e-3, lse <= 5e-3, dH/dW <= 1e-2."""
+Tolerances: |loss| <= 1e-3, relative Frobenius <= 5e-3 for dH and dW, per-row
+lse <= 1e-3 (diagnostic). fp32 inputs take the split-precision path (bf16
+hi/lo pairs, relative error about 2^-16) and meet the same bounds with room."""
 import numpy as np
 import pytest
 
@@ -83,7 +83,7 @@ def test_sampled_oracle(name):
     assert errs["dH_rows"] <= TOL_REL and errs["dW_rows"] <= TOL_REL, errs
 
 
-def test_tiny_fp32_tf32_path():
+def test_tiny_fp32_split_path():
     x = make_inputs("tiny")
     g = _gpu_run(x)
     ref = oracle.forward_backward(x.H.astype(np.float64), x.W.astype(np.float64), x.targets, IGNORE_INDEX)
@@ -92,8 +92,8 @@ def test_tiny_fp32_tf32_path():
             "lse": float(np.max(np.abs(g["lse"][valid] - ref["lse"]))),
             "dH": rel_fro(np64(g["dH"]), ref["dH"]), "dW": rel_fro(np64(g["dW"]), ref["dW"])}
     print("tiny fp32", errs)
-    assert errs["loss"] <= 2e-3 and errs["lse"] <= 5e-3, errs
-    assert errs["dH"] <= 1e-2 and errs["dW"] <= 1e-2, errs
+    assert errs["loss"] <= TOL_LOSS and errs["lse"] <= TOL_LSE, errs
+    assert errs["dH"] <= TOL_REL and errs["dW"] <= TOL_REL, errs
 
 
 def test_peak_memory_is_not_n_times_v():
