@@ -27,6 +27,8 @@ SIGNATURES = {
     "lce_forward": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int64, c_void_p, c_void_p]),
     "lce_forward_backward": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int64, c_void_p,
                                      c_void_p, c_void_p, c_void_p]),
+    "lce_forward_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int64, c_void_p,
+                                    c_void_p]),
     "lce_compact": (c_int, [c_void_p, c_int64, c_int64, c_int64, c_void_p, c_void_p, c_void_p, c_void_p]),
     "lce_run": (c_int, [c_void_p]),
     "lce_workspace_size": (c_size_t, [c_int64, c_int64, c_int64, c_int, c_int64]),

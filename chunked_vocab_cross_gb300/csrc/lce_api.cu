@@ -383,6 +383,47 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
     return LCE_OK;
 }
 
+// ------------------------------------------------------ allocation-free entry
+//
+// Scratch for lce_forward_noalloc: a fixed device array that every GPU loading
+// this library holds until the process exits. Its host-side name is only a
+// stand-in; the device address is looked up once per device.
+constexpr int64_t kNoAllocMaxN = 4096;
+constexpr int64_t kNoAllocMaxD = 2048;
+constexpr size_t kNoAllocScratchBytes = size_t(21) << 20;   // 21 MiB: bf16 Hc of 4096 x 2048 + row buffers
+
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+// Device address of g_noalloc_scratch on the current device, looked up the
+// first time each device is seen (with that device current).
+lce_status_t noalloc_scratch(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        t_last_cuda = e;
+        return LCE_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return LCE_ERR_DEVICE;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) {
+            t_last_cuda = e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+            return LCE_ERR_CUDA;
+        }
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return LCE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -532,6 +573,44 @@ lce_status_t lce_profile_end(double *ms, int64_t *launches, int n) {
     }
     t_prof.recs.clear();
     return st;
+}
+
+lce_status_t lce_forward_noalloc(const void *H, const void *W, const int64_t *targets, int64_t ignore_index,
+                                 int64_t N, int64_t d, int64_t V, float *loss, lce_stream_t stream) {
+    if (!H || !W || !targets || !loss) return LCE_ERR_NULL;
+    if (N < 1 || N > kNoAllocMaxN || d < 1 || d > kNoAllocMaxD || V < 1 || V >= (int64_t(1) << 31))
+        return LCE_ERR_SHAPE;
+    const Layout L = make_layout(N, d, V, LCE_BF16, pick_chunk(V, 0), false);
+    if (L.total > kNoAllocScratchBytes) return LCE_ERR_SHAPE;
+    DevInfo *di = nullptr;
+    lce_status_t s = device_info(&di);
+    if (s != LCE_OK) return s;
+    void *scratch = nullptr;
+    s = noalloc_scratch(&scratch);
+    if (s != LCE_OK) return s;
+    // The array keeps the previous call's contents; the compaction kernel
+    // rewrites the counters, but they are cleared first so nothing can read a
+    // stale valid-token count.
+    cudaError_t e = cudaMemsetAsync(static_cast<uint8_t *>(scratch) + L.counters, 0, 64,
+                                    reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        t_last_cuda = e;
+        return LCE_ERR_CUDA;
+    }
+    lce_args_t a{};
+    a.dtype = LCE_BF16;
+    a.H = H;
+    a.W = W;
+    a.targets = targets;
+    a.ignore_index = ignore_index;
+    a.N = N;
+    a.d = d;
+    a.V = V;
+    a.loss = loss;
+    a.workspace = scratch;
+    a.workspace_bytes = kNoAllocScratchBytes;
+    a.stream = stream;
+    return lce_run(&a);
 }
 
 int lce_version(void) { return 100; }

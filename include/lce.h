@@ -174,6 +174,27 @@ int64_t lce_launch_count(void);
 lce_status_t lce_profile_begin(void);
 lce_status_t lce_profile_end(double *ms, int64_t *launches, int n);
 
+/*
+ * Forward loss like lce_forward, for callers that must not allocate device
+ * memory: real-time or long-running loops whose memory budget is fixed up
+ * front (an allocation can stall the device or fail from fragmentation at an
+ * arbitrary point), and hosts that forbid device allocation after start-up.
+ * It calls no cudaMalloc, cudaFree or other allocating routine; the pages
+ * have no counterpart of this entry point.
+ *
+ * Scratch lives in one fixed 21 MiB device array inside the library, which
+ * every GPU that loads liblce.so holds until the process exits. Limits:
+ * N <= 4096 and d <= 2048 (LCE_ERR_SHAPE beyond them); bf16 H and W; other
+ * arguments, layout and errors as in lce_forward. The first call on each
+ * device looks up the array's device address (with that device current); make
+ * that first call before any stream capture. All calls share the one array:
+ * calls that overlap on the GPU (different streams, or different host threads
+ * on one device) race and corrupt each other's results; serialise them.
+ */
+lce_status_t lce_forward_noalloc(const void *H, const void *W, const int64_t *targets,
+                                 int64_t ignore_index, int64_t N, int64_t d, int64_t V,
+                                 float *loss, lce_stream_t stream);
+
 /* ABI version: major*10000 + minor*100 + patch. */
 int lce_version(void);
 
