@@ -286,19 +286,14 @@ def main():
     useful_flops = 6.0 * nv * w.d * w.V
     executed_flops = 8.0 * nv * w.d * w.V
     tflops_useful = useful_flops / (ms_step / 1e3) / 1e12 * 1.0
-    # dominant kernel: largest share of the profiled step time
-    gemm_phases = {"logits_lse": 1, "bwd_logits_G": 1, "dW": 1, "dH": 1}
-    name = max(gemm_phases, key=lambda k: phases[k]["ms"])
+    # dominant kernel: largest share of the profiled step time. The forward is
+    # one k_gemm<LSE> launch (2*Nv*d*V FLOPs); the backward is one k_gemm<BWD>
+    # launch per vocab chunk plus one (3 * 2*Nv*d*V FLOPs over all of them).
+    gemm_flops = {"logits_lse": 2.0 * nv * w.d * w.V, "backward": 6.0 * nv * w.d * w.V}
+    name = max(gemm_flops, key=lambda k: phases[k]["ms"])
     ph = phases[name]
     per_launch_ms = ph["ms"] / max(1, ph["launches"])
-    if name == "logits_lse":
-        flops_launch = 2.0 * nv * w.d * w.V
-    else:
-        # one launch per vocab chunk
-        n_chunks = -(-w.V // 4096)
-        kern_launches = n_chunks * prof_steps
-        per_launch_ms = ph["ms"] / kern_launches
-        flops_launch = 2.0 * nv * w.d * w.V / n_chunks
+    flops_launch = gemm_flops[name] / max(1, ph["launches"] // prof_steps)
     achieved = flops_launch / (per_launch_ms / 1e3) / 1e12
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     total_prof = sum(p["ms"] for p in phases.values())

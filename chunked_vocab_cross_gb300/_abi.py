@@ -13,8 +13,8 @@ LIB_PATH = os.path.join(_PKG, "liblce.so")
 
 LCE_BF16, LCE_FP32 = 0, 1
 LCE_DEV_TARGET_RANGE, LCE_DEV_TIMEOUT = 0x1, 0x2
-PROFILE_PHASES = 7
-PHASE_NAMES = ("compact_gather", "logits_lse", "lse_merge_loss", "bwd_logits_G", "dW", "dH", "dH_scatter")
+PROFILE_PHASES = 5
+PHASE_NAMES = ("compact_gather", "logits_lse", "lse_merge_loss", "backward", "dH_scatter")
 
 STATUS = {
     0: "LCE_OK", 1: "LCE_ERR_NULL", 2: "LCE_ERR_SHAPE", 3: "LCE_ERR_ALIGN", 4: "LCE_ERR_DTYPE",

@@ -8,16 +8,17 @@
 //   3 k_gemm<LSE>      logits tiles + online log-sum-exp partials + target logit
 //   4 k_lse_merge      lse per row, loss_i
 //   5 k_loss_reduce    loss = mean loss_i
-//   backward, per vocab chunk c of Vc rows:
-//   6 k_gemm<G>        recompute logits of the chunk, G = (softmax - onehot)/Nv
-//   7 k_gemm<DW>       dW[chunk] = G^T Hc
-//   8 k_gemm<DH>       dHacc (+)= G W[chunk]
-//   9 k_dh_scatter     dH = dHacc[inv], zero on ignored rows
+//   backward, one launch per vocab chunk j of Vc rows (j = -1 .. chunks-1):
+//   6 k_gemm<BWD>      dW[chunk j] = G_j^T Hc and dHacc (+)= G_j W[chunk j],
+//                      and G_{j+1} = (softmax - onehot)/Nv from recomputed
+//                      logits of chunk j+1 (double-buffered G)
+//   7 k_dh_scatter     dH = dHacc[inv], zero on ignored rows
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cstring>
 #include <mutex>
 #include <vector>
 
@@ -112,8 +113,7 @@ lce_status_t device_info(DevInfo **out) {
         di.major = p.major;
         di.minor = p.minor;
         if (!(di.major == 10 && di.minor == 3) || di.sms > kMaxSms) return LCE_ERR_DEVICE;
-        const void *gemms[] = {(const void *)k_gemm<MODE_LSE>, (const void *)k_gemm<MODE_G>,
-                               (const void *)k_gemm<MODE_DH>, (const void *)k_gemm<MODE_DW>};
+        const void *gemms[] = {(const void *)k_gemm<KIND_LSE>, (const void *)k_gemm<KIND_BWD>};
         for (const void *f : gemms) {
             e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
             if (e != cudaSuccess) {
@@ -190,8 +190,9 @@ Layout make_layout(int64_t N, int64_t d, int64_t V, lce_dtype_t dt, int64_t Vc, 
         L.W_lo = take(static_cast<size_t>(V) * d * 2);
     }
     if (backward) {
-        L.G = take(L.N_pad * Vc * 2);
-        if (split) L.G_lo = take(L.N_pad * Vc * 2);
+        // two G buffers: chunk j is read while chunk j+1 is written
+        L.G = take(2 * L.N_pad * Vc * 2);
+        if (split) L.G_lo = take(2 * L.N_pad * Vc * 2);
         L.dHacc = take(L.N_pad * d * 4);
     }
     L.total = o;
@@ -284,10 +285,14 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
     const __nv_bfloat16 *Hc_lo_or_hi = split ? Hc_lo : Hc;
 
     // K-major operand maps (box 64 x rows) and MN-major ones (box 64 x 64)
-    CUtensorMap tmHc_k, tmHcl_k, tmW_k, tmWl_k;
-    if (!encode_map(&tmHc_k, Hc, d, L.N_pad, kBK, kBM) || !encode_map(&tmHcl_k, Hc_lo_or_hi, d, L.N_pad, kBK, kBM) ||
-        !encode_map(&tmW_k, W_hi, d, V, kBK, kBN) || !encode_map(&tmWl_k, W_lo, d, V, kBK, kBN))
-        return LCE_ERR_CUDA;
+    GemmMaps maps_lse;
+    memset(&maps_lse, 0, sizeof(maps_lse));
+    {
+        OperandMaps &o = maps_lse.t[map_slot(T_LSE)];
+        if (!encode_map(&o.A[0], Hc, d, L.N_pad, kBK, kBM) || !encode_map(&o.A[1], Hc_lo_or_hi, d, L.N_pad, kBK, kBM) ||
+            !encode_map(&o.B[0], W_hi, d, V, kBK, kBN) || !encode_map(&o.B[1], W_lo, d, V, kBK, kBN))
+            return LCE_ERR_CUDA;
+    }
 
     GemmArgs ga{};
     ga.counters = counters;
@@ -316,11 +321,9 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
     {
         PhaseScope ph(1, st);
         GemmArgs g = ga;
-        g.v0 = 0;
-        g.vlen = V;
         g.z = z;
         g.part = part;
-        k_gemm<MODE_LSE><<<di.sms, kThreads, kGemmSmem, st>>>(tmHc_k, tmHcl_k, tmW_k, tmWl_k, g);
+        k_gemm<KIND_LSE><<<di.sms, kThreads, kGemmSmem, st>>>(maps_lse, g);
         LCE_CHECK_LAUNCH();
     }
     {
@@ -333,49 +336,55 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
     }
     if (!backward) return LCE_OK;
 
-    CUtensorMap tmG_k, tmGl_k, tmG_mn, tmGl_mn, tmHc_mn, tmHcl_mn, tmW_mn, tmWl_mn;
-    if (!encode_map(&tmG_k, G, Vc, L.N_pad, kBK, kBM) || !encode_map(&tmGl_k, G_lo, Vc, L.N_pad, kBK, kBM) ||
-        !encode_map(&tmG_mn, G, Vc, L.N_pad, kAtom, kBK) || !encode_map(&tmGl_mn, G_lo, Vc, L.N_pad, kAtom, kBK) ||
-        !encode_map(&tmHc_mn, Hc, d, L.N_pad, kAtom, kBK) ||
-        !encode_map(&tmHcl_mn, Hc_lo_or_hi, d, L.N_pad, kAtom, kBK) ||
-        !encode_map(&tmW_mn, W_hi, d, V, kAtom, kBK) || !encode_map(&tmWl_mn, W_lo, d, V, kAtom, kBK))
-        return LCE_ERR_CUDA;
-
-    for (int64_t v0 = 0; v0 < a->V; v0 += Vc) {
-        const int vlen = static_cast<int>(a->V - v0 < Vc ? a->V - v0 : Vc);
-        GemmArgs g = ga;
-        g.v0 = static_cast<int>(v0);
-        g.vlen = vlen;
-        g.ldg = static_cast<int>(Vc);
-        g.G = G;
-        g.G_lo = G_lo;
-        g.lse2 = lse2;
-        {
-            PhaseScope ph(3, st);
-            k_gemm<MODE_G><<<di.sms, kThreads, kGemmSmem, st>>>(tmHc_k, tmHcl_k, tmW_k, tmWl_k, g);
-            LCE_CHECK_LAUNCH();
-        }
-        {
-            PhaseScope ph(4, st);
-            GemmArgs gw = g;
-            gw.dW = a->dW;
-            gw.accumulate = a->accumulate_dW ? 1 : 0;
-            const int units = cdiv(vlen, kBM) * cdiv(d, kBN);
-            k_gemm<MODE_DW><<<units < di.sms ? units : di.sms, kThreads, kGemmSmem, st>>>(tmG_mn, tmGl_mn, tmHc_mn,
-                                                                                        tmHcl_mn, gw);
-            LCE_CHECK_LAUNCH();
-        }
-        {
-            PhaseScope ph(5, st);
-            GemmArgs gh = g;
-            gh.dH_acc = dHacc;
-            gh.accumulate = v0 > 0 ? 1 : 0;
-            k_gemm<MODE_DH><<<di.sms, kThreads, kGemmSmem, st>>>(tmG_k, tmGl_k, tmW_mn, tmWl_mn, gh);
+    // Backward: launch j runs dW/dH of chunk j (reading G buffer j%2) and the G
+    // tiles of chunk j+1 (writing G buffer (j+1)%2); launch j = -1 only fills G
+    // of chunk 0 and the last launch has no next chunk.
+    const size_t gbuf = static_cast<size_t>(L.N_pad) * Vc;   // elements per G buffer
+    GemmMaps maps_bwd[2];
+    memset(maps_bwd, 0, sizeof(maps_bwd));
+    for (int b = 0; b < 2; ++b) {
+        const __nv_bfloat16 *Gb = G + b * gbuf;
+        const __nv_bfloat16 *Gb_lo = G_lo + b * gbuf;
+        maps_bwd[b].t[map_slot(T_G)] = maps_lse.t[map_slot(T_LSE)];
+        OperandMaps &dh = maps_bwd[b].t[map_slot(T_DH)];
+        OperandMaps &dw = maps_bwd[b].t[map_slot(T_DW)];
+        if (!encode_map(&dh.A[0], Gb, Vc, L.N_pad, kBK, kBM) || !encode_map(&dh.A[1], Gb_lo, Vc, L.N_pad, kBK, kBM) ||
+            !encode_map(&dh.B[0], W_hi, d, V, kAtom, kBK) || !encode_map(&dh.B[1], W_lo, d, V, kAtom, kBK) ||
+            !encode_map(&dw.A[0], Gb, Vc, L.N_pad, kAtom, kBK) || !encode_map(&dw.A[1], Gb_lo, Vc, L.N_pad, kAtom, kBK) ||
+            !encode_map(&dw.B[0], Hc, d, L.N_pad, kAtom, kBK) ||
+            !encode_map(&dw.B[1], Hc_lo_or_hi, d, L.N_pad, kAtom, kBK))
+            return LCE_ERR_CUDA;
+    }
+    const int n_chunks = static_cast<int>((a->V + Vc - 1) / Vc);
+    {
+        PhaseScope ph(3, st);
+        for (int j = -1; j < n_chunks; ++j) {
+            GemmArgs g = ga;
+            g.ldg = static_cast<int>(Vc);
+            g.lse2 = lse2;
+            g.has_cur = j >= 0;
+            g.has_next = j + 1 < n_chunks;
+            if (g.has_cur) {
+                g.v0 = static_cast<int>(j * Vc);
+                g.vlen = static_cast<int>(a->V - g.v0 < Vc ? a->V - g.v0 : Vc);
+            }
+            if (g.has_next) {
+                g.v0n = static_cast<int>((j + 1) * Vc);
+                g.vlenn = static_cast<int>(a->V - g.v0n < Vc ? a->V - g.v0n : Vc);
+                const int wb = (j + 1) & 1;
+                g.G_wr = G + wb * gbuf;
+                g.G_wr_lo = G_lo + wb * gbuf;
+            }
+            g.dW = a->dW;
+            g.acc_dw = a->accumulate_dW ? 1 : 0;
+            g.dH_acc = dHacc;
+            g.acc_dh = j > 0 ? 1 : 0;
+            k_gemm<KIND_BWD><<<di.sms, kThreads, kGemmSmem, st>>>(maps_bwd[j < 0 ? 0 : (j & 1)], g);
             LCE_CHECK_LAUNCH();
         }
     }
     {
-        PhaseScope ph(6, st);
+        PhaseScope ph(4, st);
         const int grid = N < 8 * di.sms ? N : 8 * di.sms;
         k_dh_scatter<T><<<grid, 256, 0, st>>>(dHacc, inv, N, d, static_cast<T *>(a->dH));
         LCE_CHECK_LAUNCH();

@@ -1,5 +1,5 @@
-// Persistent, warp-specialised tcgen05 GEMM engine with the four fused
-// epilogues of the output-projection + cross-entropy path.
+// Persistent, warp-specialised tcgen05 GEMM engine with the fused epilogues
+// of the output-projection + cross-entropy path.
 //
 // One CTA per SM, 192 threads:
 //   warp 0      TMA producer: streams A and B k-blocks into a 4-stage
@@ -11,17 +11,18 @@
 //               TMEM lanes 32*(w%4)..+31, one tile row per thread) while the
 //               MMA thread already fills the other accumulator.
 //
-// Modes (D = A . B^T in TMEM):
-//   MODE_LSE  S = Hc . W^T      per 128-row block over a contiguous range of
-//             256-wide vocab tiles; the epilogue carries the online
-//             (max, sum) of exp over the row in registers and writes one
-//             (m, l) partial per row and range, plus the target logit.
-//   MODE_G    S = Hc . W_c^T    over one vocab chunk; the epilogue forms
-//             G = (exp(S - lse) - onehot) * scale / Nv and stores it (bf16).
-//   MODE_DW   dW_c = G^T . Hc   (M = chunk vocab rows, K = valid tokens);
-//             A and B are read MN-major straight from G and Hc.
-//   MODE_DH   dHacc (+)= G . W_c (M = valid tokens, K = chunk vocab rows);
-//             B is read MN-major straight from W.
+// Tile types (D = A . B^T in TMEM):
+//   T_LSE  S = Hc . W^T       per 128-row block over a contiguous range of
+//          256-wide vocab tiles; the epilogue carries the online (max, sum)
+//          of exp over the row in registers and writes one (m, l) partial per
+//          row and range, plus the target logit (forward).
+//   T_G    S = Hc . W_c^T     over one vocab chunk (logits recomputed in
+//          backward); the epilogue forms G = (exp(S - lse) - onehot) * scale/Nv
+//          and stores it (bf16).
+//   T_DW   dW_c = G^T . Hc    (M = chunk vocab rows, K = valid tokens); A and
+//          B are read MN-major straight from G and Hc.
+//   T_DH   dHacc (+)= G . W_c (M = valid tokens, K = chunk vocab rows); B is
+//          read MN-major straight from W.
 //
 // Split precision (fp32 inputs): every fp32 operand x is carried as two bf16
 // tensors, x = hi + lo with hi = bf16(x) and lo = bf16(x - hi), and the K loop
@@ -59,7 +60,6 @@ constexpr long long kDrainCycles = 200000000LL;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kFmtBf16 = 1u;   // operand format code of bf16 in the f16-kind descriptor
 
-enum GemmMode : int { MODE_LSE = 0, MODE_G = 1, MODE_DH = 2, MODE_DW = 3 };
 enum DevStatus : int { DEV_TARGET_RANGE = 1, DEV_TIMEOUT = 2 };
 
 // Device status word (LCE_DEV_* bits). The library is one translation unit,
@@ -95,79 +95,126 @@ __host__ __device__ inline long long lse_partial_rows(int rows_cap, int sms) {
     return (a > b ? a : b) * kBM;
 }
 
+// Tile types. KIND_LSE launches run only T_LSE; a KIND_BWD launch for vocab
+// chunk j runs the dW and dH tiles of chunk j and the G tiles of chunk j+1
+// (into the other half of a double-buffered G), which are independent of one
+// another, so one launch per chunk needs no synchronisation inside it.
+enum Kind : int { KIND_LSE = 0, KIND_BWD = 1 };
+enum TileType : int { T_LSE = 0, T_G = 1, T_DH = 2, T_DW = 3 };
+
+// Operand tensor maps per tile type: slot 0 = LSE / G (A = Hc K-major,
+// B = W K-major), slot 1 = DH (A = G K-major, B = W MN-major), slot 2 = DW
+// (A = G MN-major, B = Hc MN-major); [0] = hi (bf16) parts, [1] = lo parts.
+struct OperandMaps {
+    CUtensorMap A[2];
+    CUtensorMap B[2];
+};
+struct GemmMaps {
+    OperandMaps t[3];
+};
+
+__host__ __device__ constexpr int map_slot(int type) { return type == T_DH ? 1 : (type == T_DW ? 2 : 0); }
+
 struct GemmArgs {
     const int *counters;   // counters[0] = Nv (written by the compaction kernel)
     int d, V;
-    int v0;                // first vocab row of the chunk (0 for MODE_LSE)
-    int vlen;              // vocab rows in the chunk (V for MODE_LSE)
     int num_sms;
     int nseg;              // 1 (bf16 operands) or 3 (split-precision fp32 operands)
     int ldg;               // row stride of G in elements
     const int *tc;         // compacted targets, -1 where none
-    const float *lse2;     // per compacted row: lse / ln 2   (MODE_G)
-    float *z;              // per compacted row: target logit (MODE_LSE)
-    float2 *part;          // (m, l) partials [splits][m_blocks*128] (MODE_LSE)
-    __nv_bfloat16 *G;      // G chunk [rows][ldg], hi part     (MODE_G)
-    __nv_bfloat16 *G_lo;   // lo part when nseg == 3           (MODE_G)
-    float *dW;             // [V][d]                           (MODE_DW)
-    float *dH_acc;         // [rows][d]                        (MODE_DH)
-    int accumulate;        // DW / DH: add into the output instead of overwriting
-    float grad_scale;      // MODE_G: multiplies G
+    // KIND_LSE
+    float *z;              // per compacted row: target logit
+    float2 *part;          // (m, l) partials [splits][m_blocks*128]
+    // KIND_BWD: dW / dH tiles of the current chunk [v0, v0+vlen) (if has_cur),
+    // G tiles of the next chunk [v0n, v0n+vlenn) (if has_next)
+    int v0, vlen, v0n, vlenn, has_cur, has_next;
+    const float *lse2;     // per compacted row: lse / ln 2
+    __nv_bfloat16 *G_wr;   // next chunk's G [rows][ldg], hi part
+    __nv_bfloat16 *G_wr_lo;   // lo part when nseg == 3
+    float *dW;             // [V][d]
+    int acc_dw;            // add into dW instead of overwriting
+    float *dH_acc;         // [rows][d] fp32
+    int acc_dh;            // add into dHacc (every chunk after the first)
+    float grad_scale;      // multiplies G
 };
 
 struct Sched {
-    int m_blocks, n_tiles, k_seg, k_blocks, splits, units;
+    int units;
+    // KIND_LSE
+    int m_blocks, n_tiles, splits, kseg;
+    // KIND_BWD: task counts and shapes per type (tasks listed dW, dH, G)
+    int n_dw, n_dh, n_g, nt_d, nt_g, kseg_dw, kseg_dh, kseg_g;
 };
 
-template <int MODE>
+struct TileInfo {
+    int type, mb, nt, kseg;
+};
+
+template <int KIND>
 __device__ inline Sched make_sched(const GemmArgs &a, int nv) {
-    Sched s;
-    s.splits = 1;
-    if (MODE == MODE_LSE || MODE == MODE_G) {
+    Sched s{};
+    if (KIND == KIND_LSE) {
         s.m_blocks = cdiv(nv, kBM);
-        s.n_tiles = cdiv(a.vlen, kBN);
-        s.k_seg = cdiv(a.d, kBK);
-    } else if (MODE == MODE_DH) {
-        s.m_blocks = cdiv(nv, kBM);
-        s.n_tiles = cdiv(a.d, kBN);
-        s.k_seg = cdiv(a.vlen, kBK);
-    } else {
-        s.m_blocks = cdiv(a.vlen, kBM);
-        s.n_tiles = cdiv(a.d, kBN);
-        s.k_seg = cdiv(nv, kBK);
-    }
-    s.k_blocks = s.k_seg * a.nseg;
-    if (MODE == MODE_LSE) {
+        s.n_tiles = cdiv(a.V, kBN);
+        s.kseg = cdiv(a.d, kBK);
         s.splits = lse_splits(s.m_blocks, s.n_tiles, a.num_sms);
         s.units = s.m_blocks * s.splits;
     } else {
-        s.units = s.m_blocks * s.n_tiles;
+        s.nt_d = cdiv(a.d, kBN);
+        s.nt_g = a.has_next ? cdiv(a.vlenn, kBN) : 0;
+        s.n_dw = a.has_cur ? cdiv(a.vlen, kBM) * s.nt_d : 0;
+        s.n_dh = a.has_cur ? cdiv(nv, kBM) * s.nt_d : 0;
+        s.n_g = a.has_next ? cdiv(nv, kBM) * s.nt_g : 0;
+        s.kseg_dw = cdiv(nv, kBK);
+        s.kseg_dh = cdiv(a.vlen, kBK);
+        s.kseg_g = cdiv(a.d, kBK);
+        s.units = s.n_dw + s.n_dh + s.n_g;
     }
     return s;
 }
 
-// Unit u -> row block and [n_begin, n_end) of column tiles.
-//   LSE: split-major so CTAs running together share vocab tiles of W in L2.
-//   G, DH: column-tile-major, row blocks fastest (W / G tiles shared in L2).
-//   DW: row(vocab)-block-major, d tiles fastest (a G column block is shared).
-template <int MODE>
-__device__ inline void unit_tiles(const Sched &s, int u, int &mb, int &n0, int &n1, int &split) {
-    if (MODE == MODE_LSE) {
-        split = u / s.m_blocks;
-        mb = u % s.m_blocks;
+// Unit u -> [n0, n1) tiles. LSE units are (row block, contiguous vocab range),
+// split-major so CTAs running together share W tiles in L2; BWD units are one
+// tile each, dW first (longest K), then dH, then G, d / vocab tiles fastest.
+template <int KIND>
+__device__ inline void unit_range(const Sched &s, int u, int &n0, int &n1) {
+    if (KIND == KIND_LSE) {
+        const int split = u / s.m_blocks;
         n0 = static_cast<int>(static_cast<long long>(split) * s.n_tiles / s.splits);
         n1 = static_cast<int>(static_cast<long long>(split + 1) * s.n_tiles / s.splits);
-    } else if (MODE == MODE_DW) {
-        split = 0;
-        mb = u / s.n_tiles;
-        n0 = u % s.n_tiles;
-        n1 = n0 + 1;
     } else {
-        split = 0;
-        mb = u % s.m_blocks;
-        n0 = u / s.m_blocks;
-        n1 = n0 + 1;
+        n0 = 0;
+        n1 = 1;
     }
+}
+
+template <int KIND>
+__device__ inline TileInfo tile_info(const Sched &s, int u, int n) {
+    TileInfo t;
+    if (KIND == KIND_LSE) {
+        t.type = T_LSE;
+        t.mb = u % s.m_blocks;
+        t.nt = n;
+        t.kseg = s.kseg;
+    } else if (u < s.n_dw) {
+        t.type = T_DW;
+        t.mb = u / s.nt_d;
+        t.nt = u % s.nt_d;
+        t.kseg = s.kseg_dw;
+    } else if (u < s.n_dw + s.n_dh) {
+        const int q = u - s.n_dw;
+        t.type = T_DH;
+        t.mb = q / s.nt_d;
+        t.nt = q % s.nt_d;
+        t.kseg = s.kseg_dh;
+    } else {
+        const int q = u - s.n_dw - s.n_dh;
+        t.type = T_G;
+        t.mb = q / s.nt_g;
+        t.nt = q % s.nt_g;
+        t.kseg = s.kseg_g;
+    }
+    return t;
 }
 
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
@@ -215,14 +262,11 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const float (&
                            pack_bf16x2(g[8 * q + 4], g[8 * q + 5]), pack_bf16x2(g[8 * q + 6], g[8 * q + 7]));
 }
 
-// tmA0/tmB0 hold the bf16 (hi) operands; tmA1/tmB1 the lo parts (nseg == 3).
-template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
-    k_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
-           const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1, const GemmArgs a) {
-    constexpr bool kAmn = (MODE == MODE_DW);
-    constexpr bool kBmn = (MODE == MODE_DH || MODE == MODE_DW);
-    constexpr uint32_t kIdesc = idesc_f32acc(kFmtBf16, kBM, kBN, kAmn, kBmn);
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
+    constexpr uint32_t kIdescKK = idesc_f32acc(kFmtBf16, kBM, kBN, false, false);   // LSE, G
+    constexpr uint32_t kIdescKM = idesc_f32acc(kFmtBf16, kBM, kBN, false, true);    // DH
+    constexpr uint32_t kIdescMM = idesc_f32acc(kFmtBf16, kBM, kBN, true, true);     // DW
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -237,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int nv = a.counters[0];
-    const Sched s = make_sched<MODE>(a, nv);
+    const Sched s = make_sched<KIND>(a, nv);
     if (static_cast<int>(blockIdx.x) >= s.units) return;   // uniform over the CTA
 
     if (threadIdx.x == 0) {
@@ -254,12 +298,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
-        tma_prefetch_map(&tmA0);
-        tma_prefetch_map(&tmB0);
-        if (a.nseg > 1) {
-            tma_prefetch_map(&tmA1);
-            tma_prefetch_map(&tmB1);
-        }
+        for (int slot = 0; slot < (KIND == KIND_LSE ? 1 : 3); ++slot)
+            for (int h = 0; h < a.nseg && h < 2; ++h) {
+                tma_prefetch_map(&maps.t[slot].A[h]);
+                tma_prefetch_map(&maps.t[slot].B[h]);
+            }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
@@ -276,39 +319,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             int it = 0;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < s.units; u += gridDim.x) {
-                int mb, n0, n1, sp;
-                unit_tiles<MODE>(s, u, mb, n0, n1, sp);
-                for (int nt = n0; ok && nt < n1; ++nt) {
-                    for (int kbt = 0; kbt < s.k_blocks; ++kbt, ++it) {
+                int n0, n1;
+                unit_range<KIND>(s, u, n0, n1);
+                for (int n = n0; ok && n < n1; ++n) {
+                    const TileInfo t = tile_info<KIND>(s, u, n);
+                    const OperandMaps &om = maps.t[map_slot(t.type)];
+                    const int k_blocks = t.kseg * a.nseg;
+                    for (int kbt = 0; kbt < k_blocks; ++kbt, ++it) {
                         const int st = it % kStages;
                         if (!wait_bar(&empty[st], ((it / kStages) & 1) ^ 1, abort_flag)) {
                             ok = false;
                             break;
                         }
                         // segment 0: hi.hi, 1: hi.lo, 2: lo.hi
-                        const int seg = kbt / s.k_seg;
-                        const int kb = kbt - seg * s.k_seg;
-                        const CUtensorMap *ma = seg == 2 ? &tmA1 : &tmA0;
-                        const CUtensorMap *mbp = seg == 1 ? &tmB1 : &tmB0;
+                        const int seg = kbt / t.kseg;
+                        const int k0 = (kbt - seg * t.kseg) * kBK;
+                        const CUtensorMap *ma = &om.A[seg == 2 ? 1 : 0];
+                        const CUtensorMap *mbp = &om.B[seg == 1 ? 1 : 0];
                         mbar_arrive_expect_tx(&full[st], kStageBytes);
                         uint8_t *sa = smem + st * kStageBytes;
                         uint8_t *sb = sa + kStageA;
-                        const int k0 = kb * kBK;
-                        if (MODE == MODE_LSE || MODE == MODE_G) {
-                            tma_load_2d(sa, ma, &full[st], k0, mb * kBM);
-                            tma_load_2d(sb, mbp, &full[st], k0, a.v0 + nt * kBN);
-                        } else if (MODE == MODE_DH) {
-                            tma_load_2d(sa, ma, &full[st], k0, mb * kBM);
+                        if (t.type == T_LSE || t.type == T_G) {
+                            const int vb = (t.type == T_G ? a.v0n : 0) + t.nt * kBN;
+                            tma_load_2d(sa, ma, &full[st], k0, t.mb * kBM);
+                            tma_load_2d(sb, mbp, &full[st], k0, vb);
+                        } else if (t.type == T_DH) {
+                            tma_load_2d(sa, ma, &full[st], k0, t.mb * kBM);
 #pragma unroll
                             for (int b = 0; b < kBN / kAtom; ++b)
-                                tma_load_2d(sb + b * kAtomBytes, mbp, &full[st], nt * kBN + b * kAtom, a.v0 + k0);
+                                tma_load_2d(sb + b * kAtomBytes, mbp, &full[st], t.nt * kBN + b * kAtom, a.v0 + k0);
                         } else {
 #pragma unroll
                             for (int b = 0; b < kBM / kAtom; ++b)
-                                tma_load_2d(sa + b * kAtomBytes, ma, &full[st], mb * kBM + b * kAtom, k0);
+                                tma_load_2d(sa + b * kAtomBytes, ma, &full[st], t.mb * kBM + b * kAtom, k0);
 #pragma unroll
                             for (int b = 0; b < kBN / kAtom; ++b)
-                                tma_load_2d(sb + b * kAtomBytes, mbp, &full[st], nt * kBN + b * kAtom, k0);
+                                tma_load_2d(sb + b * kAtomBytes, mbp, &full[st], t.nt * kBN + b * kAtom, k0);
                         }
                     }
                 }
@@ -325,9 +371,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             int it = 0, tile = 0;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < s.units; u += gridDim.x) {
-                int mb, n0, n1, sp;
-                unit_tiles<MODE>(s, u, mb, n0, n1, sp);
-                for (int nt = n0; ok && nt < n1; ++nt, ++tile) {
+                int n0, n1;
+                unit_range<KIND>(s, u, n0, n1);
+                for (int n = n0; ok && n < n1; ++n, ++tile) {
+                    const TileInfo t = tile_info<KIND>(s, u, n);
+                    const bool a_mn = t.type == T_DW;
+                    const bool b_mn = t.type == T_DW || t.type == T_DH;
+                    const uint32_t idesc = a_mn ? kIdescMM : (b_mn ? kIdescKM : kIdescKK);
+                    const int k_blocks = t.kseg * a.nseg;
                     const int acc = tile & 1;
                     if (!wait_bar(&tempty[acc], ((tile >> 1) & 1) ^ 1, abort_flag)) {
                         ok = false;
@@ -335,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + acc * kBN;
-                    for (int kb = 0; kb < s.k_blocks; ++kb, ++it) {
+                    for (int kb = 0; kb < k_blocks; ++kb, ++it) {
                         const int st = it % kStages;
                         if (!wait_bar(&full[st], (it / kStages) & 1, abort_flag)) {
                             ok = false;
@@ -346,11 +397,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t sb = sa + kStageA;
 #pragma unroll
                         for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-                            const uint64_t ad = kAmn ? sdesc_sw128(sa + kk * kUmmaK * 128, kAtomBytes, 1024)
+                            const uint64_t ad = a_mn ? sdesc_sw128(sa + kk * kUmmaK * 128, kAtomBytes, 1024)
                                                      : sdesc_sw128(sa + kk * 32, 16, 1024);
-                            const uint64_t bd = kBmn ? sdesc_sw128(sb + kk * kUmmaK * 128, kAtomBytes, 1024)
+                            const uint64_t bd = b_mn ? sdesc_sw128(sb + kk * kUmmaK * 128, kAtomBytes, 1024)
                                                      : sdesc_sw128(sb + kk * 32, 16, 1024);
-                            umma_f16(d_tmem, ad, bd, kIdesc, (kb | kk) != 0);
+                            umma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
                         }
                         umma_commit(&empty[st]);   // frees the stage once these MMAs have read it
                     }
@@ -369,17 +420,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         int tile = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < s.units; u += gridDim.x) {
-            int mb, n0, n1, sp;
-            unit_tiles<MODE>(s, u, mb, n0, n1, sp);
-            const int grow = mb * kBM + trow;      // compacted row (LSE/G/DH) or chunk vocab row (DW)
-            // target column relative to the first column this launch covers (the
-            // chunk start v0 in MODE_G), negative / out of range when absent
-            int tgt = -1;
-            float lse2 = 0.f;
-            if (MODE == MODE_LSE || MODE == MODE_G) tgt = grow < nv ? a.tc[grow] - a.v0 : -1;
-            if (MODE == MODE_G) lse2 = grow < nv ? a.lse2[grow] : INFINITY;
-            float run_m = -INFINITY, run_l = 0.f;
-            for (int nt = n0; nt < n1; ++nt, ++tile) {
+            int n0, n1;
+            unit_range<KIND>(s, u, n0, n1);
+            float run_m = -INFINITY, run_l = 0.f;   // online log-sum-exp of this row over the unit (LSE)
+            int grow = 0;
+            for (int n = n0; n < n1; ++n, ++tile) {
+                const TileInfo t = tile_info<KIND>(s, u, n);
+                grow = t.mb * kBM + trow;   // compacted row (LSE/G/DH) or chunk vocab row (DW)
+                // target column relative to the first column of the vocab range
+                // this tile type covers; negative / out of range when absent
+                int tgt = -1;
+                float lse2 = INFINITY;
+                if (t.type == T_LSE) tgt = grow < nv ? a.tc[grow] : -1;
+                if (t.type == T_G && grow < nv) {
+                    tgt = a.tc[grow] - a.v0n;
+                    lse2 = a.lse2[grow];
+                }
                 const int acc = tile & 1;
                 if (!wait_bar(&tfull[acc], (tile >> 1) & 1, abort_flag)) {
                     ok = false;
@@ -392,8 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t r[32];
                     tmem_ld32(tbase + c * 32, r);
                     tmem_ld_wait();
-                    const int col = nt * kBN + c * 32;   // column within the chunk / d
-                    if (MODE == MODE_LSE) {
+                    const int col = t.nt * kBN + c * 32;   // column within the vocab range / d
+                    if (t.type == T_LSE) {
                         const int rel = tgt - col;
                         if (static_cast<unsigned>(rel) < 32u) {
                             float zv = 0.f;
@@ -406,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float cm = -INFINITY;
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
-                            x[j] = (col + j < a.vlen) ? __uint_as_float(r[j]) * kLog2e : -INFINITY;
+                            x[j] = (col + j < a.V) ? __uint_as_float(r[j]) * kLog2e : -INFINITY;
                             cm = fmaxf(cm, x[j]);
                         }
                         const float mn = fmaxf(run_m, cm);
@@ -417,32 +473,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                             run_l = run_l * exp2f(run_m - mn) + sum;
                             run_m = mn;
                         }
-                    } else if (MODE == MODE_G) {
+                    } else if (t.type == T_G) {
                         const size_t off = static_cast<size_t>(grow) * a.ldg + col;
                         float g[32];
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
                             float v = exp2f(__uint_as_float(r[j]) * kLog2e - lse2) * inv_nv;
                             if (col + j == tgt) v -= inv_nv;
-                            g[j] = (col + j < a.vlen) ? v : 0.f;
+                            g[j] = (col + j < a.vlenn) ? v : 0.f;
                         }
                         if (a.nseg == 1) {
-                            store_bf16x32(a.G + off, g);
+                            store_bf16x32(a.G_wr + off, g);
                         } else {
                             float lo[32];
 #pragma unroll
                             for (int j = 0; j < 32; ++j) split_bf16(g[j], g[j], lo[j]);
-                            store_bf16x32(a.G + off, g);
-                            store_bf16x32(a.G_lo + off, lo);
+                            store_bf16x32(a.G_wr + off, g);
+                            store_bf16x32(a.G_wr_lo + off, lo);
                         }
                     } else {
                         // DW: row = chunk vocab row, out = dW[v0 + row]; DH: row = compacted token
-                        const bool row_ok = (MODE == MODE_DW) ? (grow < a.vlen) : (grow < nv);
+                        const bool is_dw = t.type == T_DW;
+                        const bool row_ok = is_dw ? (grow < a.vlen) : (grow < nv);
                         if (row_ok && col < a.d) {
-                            float *out = (MODE == MODE_DW)
-                                             ? a.dW + static_cast<size_t>(a.v0 + grow) * a.d + col
-                                             : a.dH_acc + static_cast<size_t>(grow) * a.d + col;
-                            const bool zero_acc = (s.k_blocks == 0);
+                            float *out = is_dw ? a.dW + static_cast<size_t>(a.v0 + grow) * a.d + col
+                                               : a.dH_acc + static_cast<size_t>(grow) * a.d + col;
+                            const bool accumulate = is_dw ? a.acc_dw : a.acc_dh;
+                            const bool zero_acc = (t.kseg == 0);
                             if (col + 32 <= a.d) {
                                 float4 *o4 = reinterpret_cast<float4 *>(out);
 #pragma unroll
@@ -452,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                                       __uint_as_float(r[4 * q + 1]),
                                                                       __uint_as_float(r[4 * q + 2]),
                                                                       __uint_as_float(r[4 * q + 3]));
-                                    if (a.accumulate) {
+                                    if (accumulate) {
                                         const float4 o = o4[q];
                                         v.x += o.x;
                                         v.y += o.y;
@@ -466,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 for (int j = 0; j < 32; ++j) {
                                     if (col + j < a.d) {
                                         float v = zero_acc ? 0.f : __uint_as_float(r[j]);
-                                        if (a.accumulate) v += out[j];
+                                        if (accumulate) v += out[j];
                                         out[j] = v;
                                     }
                                 }
@@ -478,8 +535,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[acc]);
             }
-            if (MODE == MODE_LSE && ok && grow < nv)
-                a.part[static_cast<size_t>(sp) * s.m_blocks * kBM + grow] = make_float2(run_m, run_l);
+            if (KIND == KIND_LSE && ok && grow < nv) {
+                const int split = u / s.m_blocks;
+                a.part[static_cast<size_t>(split) * s.m_blocks * kBM + grow] = make_float2(run_m, run_l);
+            }
         }
     }
 

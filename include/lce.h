@@ -164,13 +164,13 @@ int64_t lce_launch_count(void);
  * Phase timing for profiling. While enabled (on the calling thread), every
  * call records CUDA events on its stream around each phase:
  *   0 compaction + gather of valid rows, 1 logits + online log-sum-exp,
- *   2 log-sum-exp merge + loss, 3 backward logits -> G, 4 dW = G^T H,
- *   5 dH accumulation G W, 6 scatter of dH to the caller's rows.
+ *   2 log-sum-exp merge + loss, 3 backward (recomputed logits -> G, dW = G^T H,
+ *   dH += G W, one launch per vocab chunk), 4 scatter of dH to the caller's rows.
  * lce_profile_end synchronises those events and returns, per phase, the summed
  * milliseconds and the number of kernel launches; it then disables timing.
  * n is the length of both output arrays (at most LCE_PROFILE_PHASES used).
  */
-#define LCE_PROFILE_PHASES 7
+#define LCE_PROFILE_PHASES 5
 lce_status_t lce_profile_begin(void);
 lce_status_t lce_profile_end(double *ms, int64_t *launches, int n);
 
