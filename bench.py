@@ -186,6 +186,9 @@ def main():
     ap.add_argument("--impl", default="lce", choices=["lce", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--vocab", type=int, default=0,
+                    help="override V (a smaller case with the same per-launch shape, for profiling)")
+    ap.add_argument("--vocab-chunk", type=int, default=0, help="backward vocab chunk (0 = library default)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
@@ -205,7 +208,10 @@ def main():
     barrier(world)
 
     # each rank draws its own batch (seed = rank): independent problems
-    x = make_inputs(args.workload, seed=rank)
+    over = {"seed": rank}
+    if args.vocab:
+        over["V"] = args.vocab
+    x = make_inputs(args.workload, **over)
     nv = int((x.targets != -100).sum())
     w = x.workload
     H_host = torch.from_numpy(x.H.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -216,10 +222,10 @@ def main():
     loss = torch.empty((), dtype=torch.float32, device=dev)
     dH = torch.empty_like(H)
     dW = torch.empty(W.shape, dtype=torch.float32, device=dev)
-    ws = torch.empty(lce.workspace_size(w.N, w.d, w.V), dtype=torch.uint8, device=dev)
+    ws = torch.empty(lce.workspace_size(w.N, w.d, w.V, vocab_chunk=args.vocab_chunk), dtype=torch.uint8, device=dev)
 
     def step():
-        lce.lce_run(H, W, t, -100, loss=loss, dH=dH, dW=dW, workspace=ws)
+        lce.lce_run(H, W, t, -100, loss=loss, dH=dH, dW=dW, workspace=ws, vocab_chunk=args.vocab_chunk)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -261,7 +267,7 @@ def main():
     def e2e_step():
         H_e.copy_(H_host, non_blocking=True)
         t_e.copy_(t_host, non_blocking=True)
-        l, _, _ = lce.lce_forward_backward(H_e, W, t_e, -100)
+        l, _, _ = lce.lce_forward_backward(H_e, W, t_e, -100, vocab_chunk=args.vocab_chunk)
         e2e_loss.copy_(l, non_blocking=True)
 
     for _ in range(2):
@@ -328,6 +334,7 @@ def main():
         "device_status": status,
         "clocks": clocks,
         "workspace_bytes": int(ws.numel()),
+        "vocab_chunk": args.vocab_chunk or 4096,
         "logits_bytes_avoided": int(w.N * w.V * 4),
     }
     print(json.dumps(line), flush=True)
