@@ -150,6 +150,24 @@ bool encode_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer
     return r == CUDA_SUCCESS;
 }
 
+// 3-D bf16 map over the same row-major [outer][inner] array for MN-major
+// operand tiles: dims {64, outer, inner/64} with strides {row, 128 bytes}, so
+// one box {64, box_rows, box_blocks} lands as box_blocks consecutive
+// {box_rows x 128-byte} blocks, the layout the MN-major descriptors read.
+// Only valid when inner is a multiple of 64 (a partial block would read into
+// the next row instead of being zero-filled).
+bool encode_map_mn3(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint32_t box_rows,
+                    uint32_t box_blocks) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kAtom), outer, inner / kAtom};
+    cuuint64_t strides[2] = {inner * 2, static_cast<cuuint64_t>(kAtom) * 2};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(kAtom), box_rows, box_blocks};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // ----------------------------------------------------------------- workspace
 
 inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -340,6 +358,7 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
     // tiles of chunk j+1 (writing G buffer (j+1)%2); launch j = -1 only fills G
     // of chunk 0 and the last launch has no next chunk.
     const size_t gbuf = static_cast<size_t>(L.N_pad) * Vc;   // elements per G buffer
+    const bool mn3d_d = (d % kAtom) == 0;
     GemmMaps maps_bwd[2];
     memset(maps_bwd, 0, sizeof(maps_bwd));
     for (int b = 0; b < 2; ++b) {
@@ -349,11 +368,20 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
         OperandMaps &dh = maps_bwd[b].t[map_slot(T_DH)];
         OperandMaps &dw = maps_bwd[b].t[map_slot(T_DW)];
         if (!encode_map(&dh.A[0], Gb, Vc, L.N_pad, kBK, kBM) || !encode_map(&dh.A[1], Gb_lo, Vc, L.N_pad, kBK, kBM) ||
-            !encode_map(&dh.B[0], W_hi, d, V, kAtom, kBK) || !encode_map(&dh.B[1], W_lo, d, V, kAtom, kBK) ||
-            !encode_map(&dw.A[0], Gb, Vc, L.N_pad, kAtom, kBK) || !encode_map(&dw.A[1], Gb_lo, Vc, L.N_pad, kAtom, kBK) ||
-            !encode_map(&dw.B[0], Hc, d, L.N_pad, kAtom, kBK) ||
-            !encode_map(&dw.B[1], Hc_lo_or_hi, d, L.N_pad, kAtom, kBK))
+            !encode_map_mn3(&dw.A[0], Gb, Vc, L.N_pad, kBK, kBM / kAtom) ||
+            !encode_map_mn3(&dw.A[1], Gb_lo, Vc, L.N_pad, kBK, kBM / kAtom))
             return LCE_ERR_CUDA;
+        if (mn3d_d) {
+            if (!encode_map_mn3(&dh.B[0], W_hi, d, V, kBK, kBN / kAtom) ||
+                !encode_map_mn3(&dh.B[1], W_lo, d, V, kBK, kBN / kAtom) ||
+                !encode_map_mn3(&dw.B[0], Hc, d, L.N_pad, kBK, kBN / kAtom) ||
+                !encode_map_mn3(&dw.B[1], Hc_lo_or_hi, d, L.N_pad, kBK, kBN / kAtom))
+                return LCE_ERR_CUDA;
+        } else if (!encode_map(&dh.B[0], W_hi, d, V, kAtom, kBK) || !encode_map(&dh.B[1], W_lo, d, V, kAtom, kBK) ||
+                   !encode_map(&dw.B[0], Hc, d, L.N_pad, kAtom, kBK) ||
+                   !encode_map(&dw.B[1], Hc_lo_or_hi, d, L.N_pad, kAtom, kBK)) {
+            return LCE_ERR_CUDA;
+        }
     }
     const int n_chunks = static_cast<int>((a->V + Vc - 1) / Vc);
     {
@@ -375,6 +403,7 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
                 g.G_wr = G + wb * gbuf;
                 g.G_wr_lo = G_lo + wb * gbuf;
             }
+            g.mn3d = 1 | (mn3d_d ? 6 : 0);
             g.dW = a->dW;
             g.acc_dw = a->accumulate_dW ? 1 : 0;
             g.dH_acc = dHacc;

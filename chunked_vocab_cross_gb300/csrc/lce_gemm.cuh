@@ -136,6 +136,11 @@ struct GemmArgs {
     float *dH_acc;         // [rows][d] fp32
     int acc_dh;            // add into dHacc (every chunk after the first)
     float grad_scale;      // multiplies G
+    // MN-major operand maps that are 3-D ({64 within a 128-byte line, K rows,
+    // 64-wide column blocks}: one box per operand per stage) instead of 2-D
+    // (one {64, 64} box per column block); 3-D needs the MN extent to be a
+    // multiple of 64. Bit 0: DW's A (G), bit 1: DW's B (Hc), bit 2: DH's B (W).
+    int mn3d;
 };
 
 struct Sched {
@@ -345,16 +350,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ge
                             tma_load_2d(sb, mbp, &full[st], k0, vb);
                         } else if (t.type == T_DH) {
                             tma_load_2d(sa, ma, &full[st], k0, t.mb * kBM);
+                            if (a.mn3d & 4) {
+                                tma_load_3d(sb, mbp, &full[st], 0, a.v0 + k0, t.nt * (kBN / kAtom));
+                            } else {
 #pragma unroll
-                            for (int b = 0; b < kBN / kAtom; ++b)
-                                tma_load_2d(sb + b * kAtomBytes, mbp, &full[st], t.nt * kBN + b * kAtom, a.v0 + k0);
+                                for (int b = 0; b < kBN / kAtom; ++b)
+                                    tma_load_2d(sb + b * kAtomBytes, mbp, &full[st], t.nt * kBN + b * kAtom,
+                                                a.v0 + k0);
+                            }
                         } else {
+                            if (a.mn3d & 1) {
+                                tma_load_3d(sa, ma, &full[st], 0, k0, t.mb * (kBM / kAtom));
+                            } else {
 #pragma unroll
-                            for (int b = 0; b < kBM / kAtom; ++b)
-                                tma_load_2d(sa + b * kAtomBytes, ma, &full[st], t.mb * kBM + b * kAtom, k0);
+                                for (int b = 0; b < kBM / kAtom; ++b)
+                                    tma_load_2d(sa + b * kAtomBytes, ma, &full[st], t.mb * kBM + b * kAtom, k0);
+                            }
+                            if (a.mn3d & 2) {
+                                tma_load_3d(sb, mbp, &full[st], 0, k0, t.nt * (kBN / kAtom));
+                            } else {
 #pragma unroll
-                            for (int b = 0; b < kBN / kAtom; ++b)
-                                tma_load_2d(sb + b * kAtomBytes, mbp, &full[st], t.nt * kBN + b * kAtom, k0);
+                                for (int b = 0; b < kBN / kAtom; ++b)
+                                    tma_load_2d(sb + b * kAtomBytes, mbp, &full[st], t.nt * kBN + b * kAtom, k0);
+                            }
                         }
                     }
                 }
