@@ -184,9 +184,9 @@ struct Layout {
 Layout make_layout(int64_t N, int64_t d, int64_t V, lce_dtype_t dt, int64_t Vc, bool backward) {
     Layout L;
     const bool split = dt == LCE_FP32;
-    L.N_pad = (N + kBM - 1) / kBM * kBM;
+    L.N_pad = (N + kPairM - 1) / kPairM * kPairM;
     L.Vc = Vc;
-    L.part_rows = lse_partial_rows(static_cast<int>(L.N_pad), kMaxSms);
+    L.part_rows = lse_partial_rows(static_cast<int>(L.N_pad), kMaxSms / 2);
     size_t o = 0;
     auto take = [&](size_t bytes) {
         size_t at = o;
@@ -308,7 +308,7 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
     {
         OperandMaps &o = maps_lse.t[map_slot(T_LSE)];
         if (!encode_map(&o.A[0], Hc, d, L.N_pad, kBK, kBM) || !encode_map(&o.A[1], Hc_lo_or_hi, d, L.N_pad, kBK, kBM) ||
-            !encode_map(&o.B[0], W_hi, d, V, kBK, kBN) || !encode_map(&o.B[1], W_lo, d, V, kBK, kBN))
+            !encode_map(&o.B[0], W_hi, d, V, kBK, kHalfN) || !encode_map(&o.B[1], W_lo, d, V, kBK, kHalfN))
             return LCE_ERR_CUDA;
     }
 
@@ -316,7 +316,9 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
     ga.counters = counters;
     ga.d = d;
     ga.V = V;
-    ga.num_sms = di.sms;
+    const int pairs = di.sms / 2;          // one CTA pair per two SMs
+    const int grid = 2 * pairs;
+    ga.num_pairs = pairs;
     ga.nseg = split ? 3 : 1;
     ga.tc = tc;
     ga.grad_scale = a->grad_scale == 0.f ? 1.f : a->grad_scale;
@@ -326,8 +328,8 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
         PhaseScope ph(0, st);
         k_compact<<<1, kCompactThreads, 0, st>>>(a->targets, N, a->ignore_index, a->V, idx, inv, counters, a->lse);
         LCE_CHECK_LAUNCH();
-        const int grid = static_cast<int>(L.N_pad < 4 * di.sms * 8 ? L.N_pad : 4 * di.sms * 8);
-        k_gather<T><<<grid, 256, 0, st>>>(static_cast<const T *>(a->H), a->targets, d, a->V, idx, counters, Hc,
+        const int ggrid = static_cast<int>(L.N_pad < 4 * di.sms * 8 ? L.N_pad : 4 * di.sms * 8);
+        k_gather<T><<<ggrid, 256, 0, st>>>(static_cast<const T *>(a->H), a->targets, d, a->V, idx, counters, Hc,
                                            Hc_lo, tc, z);
         LCE_CHECK_LAUNCH();
         if (split) {
@@ -341,12 +343,12 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
         GemmArgs g = ga;
         g.z = z;
         g.part = part;
-        k_gemm<KIND_LSE><<<di.sms, kThreads, kGemmSmem, st>>>(maps_lse, g);
+        k_gemm<KIND_LSE><<<grid, kThreads, kGemmSmem, st>>>(maps_lse, g);
         LCE_CHECK_LAUNCH();
     }
     {
         PhaseScope ph(2, st);
-        k_lse_merge<<<static_cast<int>(L.N_pad / 256 + 1), 256, 0, st>>>(part, counters, n_tiles_v, di.sms, z, lse2,
+        k_lse_merge<<<static_cast<int>(L.N_pad / 256 + 1), 256, 0, st>>>(part, counters, n_tiles_v, pairs, z, lse2,
                                                                          loss_rows, idx, a->lse);
         LCE_CHECK_LAUNCH();
         k_loss_reduce<<<1, 1024, 0, st>>>(loss_rows, counters, a->loss);
@@ -372,10 +374,10 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
             !encode_map_mn3(&dw.A[1], Gb_lo, Vc, L.N_pad, kBK, kBM / kAtom))
             return LCE_ERR_CUDA;
         if (mn3d_d) {
-            if (!encode_map_mn3(&dh.B[0], W_hi, d, V, kBK, kBN / kAtom) ||
-                !encode_map_mn3(&dh.B[1], W_lo, d, V, kBK, kBN / kAtom) ||
-                !encode_map_mn3(&dw.B[0], Hc, d, L.N_pad, kBK, kBN / kAtom) ||
-                !encode_map_mn3(&dw.B[1], Hc_lo_or_hi, d, L.N_pad, kBK, kBN / kAtom))
+            if (!encode_map_mn3(&dh.B[0], W_hi, d, V, kBK, kHalfN / kAtom) ||
+                !encode_map_mn3(&dh.B[1], W_lo, d, V, kBK, kHalfN / kAtom) ||
+                !encode_map_mn3(&dw.B[0], Hc, d, L.N_pad, kBK, kHalfN / kAtom) ||
+                !encode_map_mn3(&dw.B[1], Hc_lo_or_hi, d, L.N_pad, kBK, kHalfN / kAtom))
                 return LCE_ERR_CUDA;
         } else if (!encode_map(&dh.B[0], W_hi, d, V, kAtom, kBK) || !encode_map(&dh.B[1], W_lo, d, V, kAtom, kBK) ||
                    !encode_map(&dw.B[0], Hc, d, L.N_pad, kAtom, kBK) ||
@@ -408,14 +410,14 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
             g.acc_dw = a->accumulate_dW ? 1 : 0;
             g.dH_acc = dHacc;
             g.acc_dh = j > 0 ? 1 : 0;
-            k_gemm<KIND_BWD><<<di.sms, kThreads, kGemmSmem, st>>>(maps_bwd[j < 0 ? 0 : (j & 1)], g);
+            k_gemm<KIND_BWD><<<grid, kThreads, kGemmSmem, st>>>(maps_bwd[j < 0 ? 0 : (j & 1)], g);
             LCE_CHECK_LAUNCH();
         }
     }
     {
         PhaseScope ph(4, st);
-        const int grid = N < 8 * di.sms ? N : 8 * di.sms;
-        k_dh_scatter<T><<<grid, 256, 0, st>>>(dHacc, inv, N, d, static_cast<T *>(a->dH));
+        const int sgrid = N < 8 * di.sms ? N : 8 * di.sms;
+        k_dh_scatter<T><<<sgrid, 256, 0, st>>>(dHacc, inv, N, d, static_cast<T *>(a->dH));
         LCE_CHECK_LAUNCH();
     }
     return LCE_OK;

@@ -1,12 +1,15 @@
 // Persistent, warp-specialised tcgen05 GEMM engine with the fused epilogues
 // of the output-projection + cross-entropy path.
 //
-// One CTA per SM, 192 threads:
-//   warp 0      TMA producer: streams A and B k-blocks into a 4-stage
-//               shared-memory ring (128-byte swizzle), signalling mbarriers.
-//   warp 1      owns TMEM (512 columns = two 128x256 fp32 accumulators) and
-//               issues tcgen05.mma.kind::f16 128x256x16 (bf16 in, fp32
-//               accumulate) from one thread.
+// One CTA per SM; CTA pairs (clusters of 2) share each 256x256 tile; 192
+// threads per CTA:
+//   warp 0      TMA producer: streams this CTA's 128 A rows and 128 of the
+//               256 B rows per k-block into a 6-stage shared-memory ring
+//               (128-byte swizzle); both CTAs signal the even CTA's barrier.
+//   warp 1      allocates TMEM (512 columns = two 128x256 fp32 accumulators
+//               per CTA); on the even CTA one thread issues
+//               tcgen05.mma.cta_group::2.kind::f16 256x256x16 (bf16 in, fp32
+//               accumulate) reading both CTAs' shared memory.
 //   warps 2..5  epilogue: tcgen05.ld the finished accumulator (warp w reads
 //               TMEM lanes 32*(w%4)..+31, one tile row per thread) while the
 //               MMA thread already fills the other accumulator.
@@ -42,18 +45,21 @@
 
 namespace lce {
 
-constexpr int kBM = 128;          // tile rows   (UMMA M)
-constexpr int kBN = 256;          // tile cols   (UMMA N)
+constexpr int kBM = 128;          // tile rows held by one CTA (TMEM lanes)
+constexpr int kPairM = 256;       // tile rows of a CTA pair (UMMA M with cta_group::2)
+constexpr int kBN = 256;          // tile cols (UMMA N), split 128 + 128 across the pair
+constexpr int kHalfN = 128;       // B rows (N) loaded by each CTA of the pair
 constexpr int kBK = 64;           // k per stage: one 128-byte bf16 line
 constexpr int kUmmaK = 16;        // k per tcgen05.mma (bf16)
 constexpr int kAtom = 64;         // MN elements per 128-byte line
 constexpr int kAtomBytes = kBK * 128;   // one MN-major box {64 (MN), 64 (K)} = 8 KB
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;    // two 256-column fp32 accumulators
-constexpr int kStageA = kBM * 128;
-constexpr int kStageB = kBN * 128;
+constexpr int kStageA = kBM * 128;      // this CTA's 128 A rows x 64 k
+constexpr int kStageB = kHalfN * 128;   // this CTA's 128 B rows x 64 k
 constexpr int kStageBytes = kStageA + kStageB;
+constexpr int kPairTx = 2 * kStageBytes;   // bytes both CTAs land on the even CTA's full barrier
 constexpr int kGemmSmem = kStages * kStageBytes + 1024 /*alignment slack*/ + 256 /*barriers*/;
 constexpr long long kWaitCycles = 2000000000LL;   // ~1 s: far above any legitimate wait
 constexpr long long kDrainCycles = 200000000LL;
@@ -68,9 +74,10 @@ __device__ int g_status = 0;
 
 __host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-// Vocab splits for MODE_LSE: choose the number of contiguous vocab ranges per
-// row block so that m_blocks*splits units fill whole waves of `sms` CTAs with
-// the shortest longest-CTA time, ceil(units/sms) * ceil(n_tiles/splits).
+// Vocab splits for the LSE pass: choose the number of contiguous vocab ranges
+// per 256-row block so that m_blocks*splits units fill whole waves of `sms`
+// CTA pairs with the shortest longest-pair time,
+// ceil(units/sms) * ceil(n_tiles/splits).
 __host__ __device__ inline int lse_splits(int m_blocks, int n_tiles, int sms) {
     if (m_blocks <= 0 || n_tiles <= 1) return 1;
     int best = 1;
@@ -88,11 +95,11 @@ __host__ __device__ inline int lse_splits(int m_blocks, int n_tiles, int sms) {
     return best;
 }
 
-// Largest number of (m, l) partial rows MODE_LSE can write for row capacity
-// `rows_cap` (a multiple of 128).
-__host__ __device__ inline long long lse_partial_rows(int rows_cap, int sms) {
-    long long a = 16LL * sms, b = rows_cap / kBM;
-    return (a > b ? a : b) * kBM;
+// Largest number of (m, l) partial rows the LSE pass can write for row
+// capacity `rows_cap` (a multiple of 256) and `pairs` CTA pairs.
+__host__ __device__ inline long long lse_partial_rows(int rows_cap, int pairs) {
+    long long a = 16LL * pairs, b = rows_cap / kPairM;
+    return (a > b ? a : b) * kPairM;
 }
 
 // Tile types. KIND_LSE launches run only T_LSE; a KIND_BWD launch for vocab
@@ -118,7 +125,7 @@ __host__ __device__ constexpr int map_slot(int type) { return type == T_DH ? 1 :
 struct GemmArgs {
     const int *counters;   // counters[0] = Nv (written by the compaction kernel)
     int d, V;
-    int num_sms;
+    int num_pairs;         // CTA pairs in the grid (gridDim.x / 2)
     int nseg;              // 1 (bf16 operands) or 3 (split-precision fp32 operands)
     int ldg;               // row stride of G in elements
     const int *tc;         // compacted targets, -1 where none
@@ -159,17 +166,17 @@ template <int KIND>
 __device__ inline Sched make_sched(const GemmArgs &a, int nv) {
     Sched s{};
     if (KIND == KIND_LSE) {
-        s.m_blocks = cdiv(nv, kBM);
+        s.m_blocks = cdiv(nv, kPairM);
         s.n_tiles = cdiv(a.V, kBN);
         s.kseg = cdiv(a.d, kBK);
-        s.splits = lse_splits(s.m_blocks, s.n_tiles, a.num_sms);
+        s.splits = lse_splits(s.m_blocks, s.n_tiles, a.num_pairs);
         s.units = s.m_blocks * s.splits;
     } else {
         s.nt_d = cdiv(a.d, kBN);
         s.nt_g = a.has_next ? cdiv(a.vlenn, kBN) : 0;
-        s.n_dw = a.has_cur ? cdiv(a.vlen, kBM) * s.nt_d : 0;
-        s.n_dh = a.has_cur ? cdiv(nv, kBM) * s.nt_d : 0;
-        s.n_g = a.has_next ? cdiv(nv, kBM) * s.nt_g : 0;
+        s.n_dw = a.has_cur ? cdiv(a.vlen, kPairM) * s.nt_d : 0;
+        s.n_dh = a.has_cur ? cdiv(nv, kPairM) * s.nt_d : 0;
+        s.n_g = a.has_next ? cdiv(nv, kPairM) * s.nt_g : 0;
         s.kseg_dw = cdiv(nv, kBK);
         s.kseg_dh = cdiv(a.vlen, kBK);
         s.kseg_g = cdiv(a.d, kBK);
@@ -178,7 +185,7 @@ __device__ inline Sched make_sched(const GemmArgs &a, int nv) {
     return s;
 }
 
-// Unit u -> [n0, n1) tiles. LSE units are (row block, contiguous vocab range),
+// Unit u -> [n0, n1) tiles. LSE units are (256-row block, contiguous vocab range),
 // split-major so CTAs running together share W tiles in L2; BWD units are one
 // tile each, dW first (longest K), then dH, then G, d / vocab tiles fastest.
 template <int KIND>
@@ -267,27 +274,37 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const float (&
                            pack_bf16x2(g[8 * q + 4], g[8 * q + 5]), pack_bf16x2(g[8 * q + 6], g[8 * q + 7]));
 }
 
+// One CTA pair (cluster of 2) per two SMs. Each CTA loads its 128 A rows and
+// its 128 of the 256 B rows per stage; the even CTA waits for both halves on
+// its full barrier, issues tcgen05.mma.cta_group::2 (M = 256, N = 256) and
+// commits stage releases and accumulator-ready signals to both CTAs; each
+// CTA's epilogue reads its own 128 rows from its TMEM and releases the
+// accumulator with an arrive on the even CTA's barrier.
 template <int KIND>
-__global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
-    constexpr uint32_t kIdescKK = idesc_f32acc(kFmtBf16, kBM, kBN, false, false);   // LSE, G
-    constexpr uint32_t kIdescKM = idesc_f32acc(kFmtBf16, kBM, kBN, false, true);    // DH
-    constexpr uint32_t kIdescMM = idesc_f32acc(kFmtBf16, kBM, kBN, true, true);     // DW
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    k_gemm(const __grid_constant__ GemmMaps maps, const GemmArgs a) {
+    constexpr uint32_t kIdescKK = idesc_f32acc(kFmtBf16, kPairM, kBN, false, false);   // LSE, G
+    constexpr uint32_t kIdescKM = idesc_f32acc(kFmtBf16, kPairM, kBN, false, true);    // DH
+    constexpr uint32_t kIdescMM = idesc_f32acc(kFmtBf16, kPairM, kBN, true, true);     // DW
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);   // used on the even CTA
     uint64_t *empty = full + kStages;
     uint64_t *tfull = empty + kStages;
-    uint64_t *tempty = tfull + 2;
+    uint64_t *tempty = tfull + 2;                                                   // used on the even CTA
     uint64_t *mma_done = tempty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();   // 0 = even CTA (issues the MMAs), 1 = its peer
+    const int pair = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
     const int nv = a.counters[0];
     const Sched s = make_sched<KIND>(a, nv);
-    if (static_cast<int>(blockIdx.x) >= s.units) return;   // uniform over the CTA
+    if (pair >= s.units) return;   // uniform over both CTAs of the pair
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -296,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ge
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], 4);
+            mbar_init(&tempty[i], 8);   // 4 epilogue warps in each CTA of the pair
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -310,20 +327,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ge
             }
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
+        tmem_alloc_pair(tmem_slot, kTmemCols);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();   // barrier inits and the TMEM allocation are visible to both CTAs
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // the even CTA's full and tempty barriers, as shared::cluster addresses
+    const uint32_t full_even = map_to_cta(smem_u32(full), 0);
+    const uint32_t tempty_even = map_to_cta(smem_u32(tempty), 0);
 
     if (warp == 0) {
         // ------------------------------------------------------- TMA producer
         if (lane == 0) {
             int it = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < s.units; u += gridDim.x) {
+            const int arow = static_cast<int>(rank) * kBM;      // this CTA's A rows within the pair tile
+            const int brow = static_cast<int>(rank) * kHalfN;   // this CTA's B rows (N) within the tile
+            for (int u = pair; ok && u < s.units; u += npairs) {
                 int n0, n1;
                 unit_range<KIND>(s, u, n0, n1);
                 for (int n = n0; ok && n < n1; ++n) {
@@ -341,54 +363,56 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ge
                         const int k0 = (kbt - seg * t.kseg) * kBK;
                         const CUtensorMap *ma = &om.A[seg == 2 ? 1 : 0];
                         const CUtensorMap *mbp = &om.B[seg == 1 ? 1 : 0];
-                        mbar_arrive_expect_tx(&full[st], kStageBytes);
+                        if (rank == 0) mbar_arrive_expect_tx(&full[st], kPairTx);
+                        const uint32_t fb = full_even + st * 8;
                         uint8_t *sa = smem + st * kStageBytes;
                         uint8_t *sb = sa + kStageA;
+                        const int am = t.mb * kPairM + arow;   // first A row (M) of this CTA
+                        const int bn = t.nt * kBN + brow;      // first B row (N) of this CTA
                         if (t.type == T_LSE || t.type == T_G) {
-                            const int vb = (t.type == T_G ? a.v0n : 0) + t.nt * kBN;
-                            tma_load_2d(sa, ma, &full[st], k0, t.mb * kBM);
-                            tma_load_2d(sb, mbp, &full[st], k0, vb);
+                            const int vb = (t.type == T_G ? a.v0n : 0) + bn;
+                            tma_load_2d_pair(sa, ma, fb, k0, am);
+                            tma_load_2d_pair(sb, mbp, fb, k0, vb);
                         } else if (t.type == T_DH) {
-                            tma_load_2d(sa, ma, &full[st], k0, t.mb * kBM);
+                            tma_load_2d_pair(sa, ma, fb, k0, am);
                             if (a.mn3d & 4) {
-                                tma_load_3d(sb, mbp, &full[st], 0, a.v0 + k0, t.nt * (kBN / kAtom));
+                                tma_load_3d_pair(sb, mbp, fb, 0, a.v0 + k0, bn / kAtom);
                             } else {
 #pragma unroll
-                                for (int b = 0; b < kBN / kAtom; ++b)
-                                    tma_load_2d(sb + b * kAtomBytes, mbp, &full[st], t.nt * kBN + b * kAtom,
-                                                a.v0 + k0);
+                                for (int b = 0; b < kHalfN / kAtom; ++b)
+                                    tma_load_2d_pair(sb + b * kAtomBytes, mbp, fb, bn + b * kAtom, a.v0 + k0);
                             }
                         } else {
                             if (a.mn3d & 1) {
-                                tma_load_3d(sa, ma, &full[st], 0, k0, t.mb * (kBM / kAtom));
+                                tma_load_3d_pair(sa, ma, fb, 0, k0, am / kAtom);
                             } else {
 #pragma unroll
                                 for (int b = 0; b < kBM / kAtom; ++b)
-                                    tma_load_2d(sa + b * kAtomBytes, ma, &full[st], t.mb * kBM + b * kAtom, k0);
+                                    tma_load_2d_pair(sa + b * kAtomBytes, ma, fb, am + b * kAtom, k0);
                             }
                             if (a.mn3d & 2) {
-                                tma_load_3d(sb, mbp, &full[st], 0, k0, t.nt * (kBN / kAtom));
+                                tma_load_3d_pair(sb, mbp, fb, 0, k0, bn / kAtom);
                             } else {
 #pragma unroll
-                                for (int b = 0; b < kBN / kAtom; ++b)
-                                    tma_load_2d(sb + b * kAtomBytes, mbp, &full[st], t.nt * kBN + b * kAtom, k0);
+                                for (int b = 0; b < kHalfN / kAtom; ++b)
+                                    tma_load_2d_pair(sb + b * kAtomBytes, mbp, fb, bn + b * kAtom, k0);
                             }
                         }
                     }
                 }
             }
-            if (!ok) {
-                // let the copies already issued land before the CTA exits
+            if (!ok && rank == 0) {
+                // let the copies already issued (by both CTAs) land before the pair exits
                 const int first = it > kStages ? it - kStages : 0;
                 for (int j = first; j < it; ++j) drain_bar(&full[j % kStages], (j / kStages) & 1);
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issue
-        if (lane == 0) {
+        // ------------------------------------------- MMA issue (even CTA only)
+        if (lane == 0 && rank == 0) {
             int it = 0, tile = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < s.units; u += gridDim.x) {
+            for (int u = pair; ok && u < s.units; u += npairs) {
                 int n0, n1;
                 unit_range<KIND>(s, u, n0, n1);
                 for (int n = n0; ok && n < n1; ++n, ++tile) {
@@ -419,32 +443,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ge
                                                      : sdesc_sw128(sa + kk * 32, 16, 1024);
                             const uint64_t bd = b_mn ? sdesc_sw128(sb + kk * kUmmaK * 128, kAtomBytes, 1024)
                                                      : sdesc_sw128(sb + kk * 32, 16, 1024);
-                            umma_f16(d_tmem, ad, bd, idesc, (kb | kk) != 0);
+                            umma_f16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0);
                         }
-                        umma_commit(&empty[st]);   // frees the stage once these MMAs have read it
+                        umma_commit_pair_mc(&empty[st], 3);   // frees the stage in both CTAs
                     }
                     if (!ok) break;
-                    umma_commit(&tfull[acc]);      // accumulator ready for the epilogue
+                    umma_commit_pair_mc(&tfull[acc], 3);      // accumulator ready in both CTAs
                 }
             }
-            umma_commit(mma_done);
+            umma_commit_pair_mc(mma_done, 1);
             drain_bar(mma_done, 0);
         }
     } else {
         // ------------------------------------------------------------ epilogue
         const int quarter = warp & 3;
-        const int trow = quarter * 32 + lane;     // row within the tile == TMEM lane
+        const int trow = quarter * 32 + lane;     // row within this CTA's 128 rows == TMEM lane
         const float inv_nv = nv > 0 ? a.grad_scale / static_cast<float>(nv) : 0.f;
         int tile = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < s.units; u += gridDim.x) {
+        for (int u = pair; ok && u < s.units; u += npairs) {
             int n0, n1;
             unit_range<KIND>(s, u, n0, n1);
             float run_m = -INFINITY, run_l = 0.f;   // online log-sum-exp of this row over the unit (LSE)
             int grow = 0;
             for (int n = n0; n < n1; ++n, ++tile) {
                 const TileInfo t = tile_info<KIND>(s, u, n);
-                grow = t.mb * kBM + trow;   // compacted row (LSE/G/DH) or chunk vocab row (DW)
+                // compacted row (LSE/G/DH) or chunk vocab row (DW) of this thread
+                grow = t.mb * kPairM + static_cast<int>(rank) * kBM + trow;
                 // target column relative to the first column of the vocab range
                 // this tile type covers; negative / out of range when absent
                 int tgt = -1;
@@ -551,19 +576,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm(const __grid_constant__ Ge
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[acc]);
+                if (lane == 0) mbar_arrive_cluster(tempty_even + acc * 8);
             }
             if (KIND == KIND_LSE && ok && grow < nv) {
                 const int split = u / s.m_blocks;
-                a.part[static_cast<size_t>(split) * s.m_blocks * kBM + grow] = make_float2(run_m, run_l);
+                a.part[static_cast<size_t>(split) * s.m_blocks * kPairM + grow] = make_float2(run_m, run_l);
             }
         }
     }
 
-    __syncthreads();
+    // Both CTAs stay resident until every remote arrive, multicast commit and
+    // copy aimed at either of them has landed; then the pair frees its TMEM.
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync_all();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        tmem_dealloc_pair(tmem_base, kTmemCols);
     }
 }
 

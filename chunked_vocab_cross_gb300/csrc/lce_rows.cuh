@@ -68,8 +68,8 @@ __global__ void __launch_bounds__(kCompactThreads)
     }
 }
 
-// Hc[r] = H[idx[r]] for r < Nv, zero rows on [Nv, round_up(Nv, 128)) so the
-// tensor-core passes can read whole 128-row blocks; tc[r] = target (or -1),
+// Hc[r] = H[idx[r]] for r < Nv, zero rows on [Nv, round_up(Nv, 256)) so the
+// tensor-core passes can read whole 256-row pair blocks; tc[r] = target (or -1),
 // z[r] = NaN until the logits pass finds the target column. bf16 rows are
 // copied; fp32 rows are split into bf16 hi and lo parts (Hc, Hc_lo).
 __device__ __forceinline__ void gather8(const __nv_bfloat16 *src, __nv_bfloat16 *hi, __nv_bfloat16 *, bool live) {
@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(256)
              const int *__restrict__ counters, __nv_bfloat16 *__restrict__ Hc, __nv_bfloat16 *__restrict__ Hc_lo,
              int *__restrict__ tc, float *__restrict__ z) {
     const int nv = counters[0];
-    const int rows = cdiv(nv, kBM) * kBM;
+    const int rows = cdiv(nv, kPairM) * kPairM;
     const int groups = d / 8;   // d is a multiple of 8
     for (int r = blockIdx.x; r < rows; r += gridDim.x) {
         const bool live = r < nv;
@@ -128,15 +128,15 @@ __global__ void __launch_bounds__(256)
 // Merge the per-range (m, l) partials of each row (log2 units) in fixed range
 // order: lse2 = M + log2(sum_s l_s 2^(m_s - M)), then loss_i = lse - z_i.
 __global__ void __launch_bounds__(256)
-    k_lse_merge(const float2 *__restrict__ part, const int *__restrict__ counters, int n_tiles, int num_sms,
+    k_lse_merge(const float2 *__restrict__ part, const int *__restrict__ counters, int n_tiles, int num_pairs,
                 const float *__restrict__ z, float *__restrict__ lse2_out, float *__restrict__ loss_rows,
                 const int *__restrict__ idx, float *__restrict__ lse_user) {
     const int nv = counters[0];
     const int row = blockIdx.x * blockDim.x + threadIdx.x;
     if (row >= nv) return;
-    const int m_blocks = cdiv(nv, kBM);
-    const int splits = lse_splits(m_blocks, n_tiles, num_sms);
-    const size_t stride = static_cast<size_t>(m_blocks) * kBM;
+    const int m_blocks = cdiv(nv, kPairM);
+    const int splits = lse_splits(m_blocks, n_tiles, num_pairs);
+    const size_t stride = static_cast<size_t>(m_blocks) * kPairM;
     float M = -INFINITY;
     for (int s = 0; s < splits; ++s) M = fmaxf(M, part[s * stride + row].x);
     float L = 0.f;
