@@ -274,6 +274,41 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const float (&
                            pack_bf16x2(g[8 * q + 4], g[8 * q + 5]), pack_bf16x2(g[8 * q + 6], g[8 * q + 7]));
 }
 
+// Issue this CTA's TMA loads of one k-block (A rows am.., B rows bn.., k0..)
+// of tile t into stage (sa, sb), completing on the even CTA's barrier fb.
+__device__ __forceinline__ void load_operands(const TileInfo &t, const GemmArgs &a, const CUtensorMap *ma,
+                                              const CUtensorMap *mbp, uint8_t *sa, uint8_t *sb, uint32_t fb, int am,
+                                              int bn, int k0) {
+    if (t.type == T_LSE || t.type == T_G) {
+        const int vb = (t.type == T_G ? a.v0n : 0) + bn;
+        tma_load_2d_pair(sa, ma, fb, k0, am);
+        tma_load_2d_pair(sb, mbp, fb, k0, vb);
+    } else if (t.type == T_DH) {
+        tma_load_2d_pair(sa, ma, fb, k0, am);
+        if (a.mn3d & 4) {
+            tma_load_3d_pair(sb, mbp, fb, 0, a.v0 + k0, bn / kAtom);
+        } else {
+#pragma unroll
+            for (int b = 0; b < kHalfN / kAtom; ++b)
+                tma_load_2d_pair(sb + b * kAtomBytes, mbp, fb, bn + b * kAtom, a.v0 + k0);
+        }
+    } else {
+        if (a.mn3d & 1) {
+            tma_load_3d_pair(sa, ma, fb, 0, k0, am / kAtom);
+        } else {
+#pragma unroll
+            for (int b = 0; b < kBM / kAtom; ++b) tma_load_2d_pair(sa + b * kAtomBytes, ma, fb, am + b * kAtom, k0);
+        }
+        if (a.mn3d & 2) {
+            tma_load_3d_pair(sb, mbp, fb, 0, k0, bn / kAtom);
+        } else {
+#pragma unroll
+            for (int b = 0; b < kHalfN / kAtom; ++b)
+                tma_load_2d_pair(sb + b * kAtomBytes, mbp, fb, bn + b * kAtom, k0);
+        }
+    }
+}
+
 // One CTA pair (cluster of 2) per two SMs. Each CTA loads its 128 A rows and
 // its 128 of the 256 B rows per stage; the even CTA waits for both halves on
 // its full barrier, issues tcgen05.mma.cta_group::2 (M = 256, N = 256) and
@@ -369,35 +404,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         uint8_t *sb = sa + kStageA;
                         const int am = t.mb * kPairM + arow;   // first A row (M) of this CTA
                         const int bn = t.nt * kBN + brow;      // first B row (N) of this CTA
-                        if (t.type == T_LSE || t.type == T_G) {
-                            const int vb = (t.type == T_G ? a.v0n : 0) + bn;
-                            tma_load_2d_pair(sa, ma, fb, k0, am);
-                            tma_load_2d_pair(sb, mbp, fb, k0, vb);
-                        } else if (t.type == T_DH) {
-                            tma_load_2d_pair(sa, ma, fb, k0, am);
-                            if (a.mn3d & 4) {
-                                tma_load_3d_pair(sb, mbp, fb, 0, a.v0 + k0, bn / kAtom);
-                            } else {
-#pragma unroll
-                                for (int b = 0; b < kHalfN / kAtom; ++b)
-                                    tma_load_2d_pair(sb + b * kAtomBytes, mbp, fb, bn + b * kAtom, a.v0 + k0);
-                            }
-                        } else {
-                            if (a.mn3d & 1) {
-                                tma_load_3d_pair(sa, ma, fb, 0, k0, am / kAtom);
-                            } else {
-#pragma unroll
-                                for (int b = 0; b < kBM / kAtom; ++b)
-                                    tma_load_2d_pair(sa + b * kAtomBytes, ma, fb, am + b * kAtom, k0);
-                            }
-                            if (a.mn3d & 2) {
-                                tma_load_3d_pair(sb, mbp, fb, 0, k0, bn / kAtom);
-                            } else {
-#pragma unroll
-                                for (int b = 0; b < kHalfN / kAtom; ++b)
-                                    tma_load_2d_pair(sb + b * kAtomBytes, mbp, fb, bn + b * kAtom, k0);
-                            }
-                        }
+                        load_operands(t, a, ma, mbp, sa, sb, fb, am, bn, k0);
                     }
                 }
             }
