@@ -9,9 +9,10 @@
 //   4 k_lse_merge      lse per row, loss_i
 //   5 k_loss_reduce    loss = mean loss_i
 //   backward, one launch per vocab chunk j of Vc rows (j = -1 .. chunks-1):
-//   6 k_gemm<BWD>      dW[chunk j] = G_j^T Hc and dHacc (+)= G_j W[chunk j],
-//                      and G_{j+1} = (softmax - onehot)/Nv from recomputed
-//                      logits of chunk j+1 (double-buffered G)
+//   6 k_gemm<BWD>      G_{j+1} = (softmax - onehot)/Nv from recomputed logits
+//                      of chunk j+1, dW[chunk j] = G_j^T Hc and
+//                      dHacc (+)= G_j W[chunk j] (three G buffers; consecutive
+//                      launches overlap through programmatic dependent launch)
 //   7 k_dh_scatter     dH = dHacc[inv], zero on ignored rows
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -33,6 +34,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kMaxSms = 256;              // bound used to size the (m, l) partials
 constexpr int64_t kDefaultVocabChunk = 4096;
+constexpr int kGBuffers = 3;
 
 thread_local int t_last_cuda = 0;
 std::atomic<int64_t> g_launches{0};
@@ -208,9 +210,10 @@ Layout make_layout(int64_t N, int64_t d, int64_t V, lce_dtype_t dt, int64_t Vc, 
         L.W_lo = take(static_cast<size_t>(V) * d * 2);
     }
     if (backward) {
-        // two G buffers: chunk j is read while chunk j+1 is written
-        L.G = take(2 * L.N_pad * Vc * 2);
-        if (split) L.G_lo = take(2 * L.N_pad * Vc * 2);
+        // three G buffers: chunk j is read while chunk j+1 is written, and the
+        // launch after may already write chunk j+2 while chunk j's last tiles run
+        L.G = take(kGBuffers * L.N_pad * Vc * 2);
+        if (split) L.G_lo = take(kGBuffers * L.N_pad * Vc * 2);
         L.dHacc = take(L.N_pad * d * 4);
     }
     L.total = o;
@@ -356,14 +359,19 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
     }
     if (!backward) return LCE_OK;
 
-    // Backward: launch j runs dW/dH of chunk j (reading G buffer j%2) and the G
-    // tiles of chunk j+1 (writing G buffer (j+1)%2); launch j = -1 only fills G
-    // of chunk 0 and the last launch has no next chunk.
+    // Backward: launch j runs the G tiles of chunk j+1 (writing G buffer
+    // (j+1)%3) and dW/dH of chunk j (reading buffer j%3); launch j = -1 only
+    // fills G of chunk 0 and the last launch has no next chunk. Launches after
+    // the first are programmatic dependents of their predecessor: their CTAs
+    // start as the predecessor's finish, and wait for it (griddepcontrol.wait)
+    // before their dW/dH tiles. A launch signals its own dependent only after
+    // that wait, so launch j+1 (writing buffer (j+2)%3 = (j-1)%3) cannot start
+    // before launch j-1, the last reader of that buffer, has completed.
     const size_t gbuf = static_cast<size_t>(L.N_pad) * Vc;   // elements per G buffer
     const bool mn3d_d = (d % kAtom) == 0;
-    GemmMaps maps_bwd[2];
+    GemmMaps maps_bwd[kGBuffers];
     memset(maps_bwd, 0, sizeof(maps_bwd));
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kGBuffers; ++b) {
         const __nv_bfloat16 *Gb = G + b * gbuf;
         const __nv_bfloat16 *Gb_lo = G_lo + b * gbuf;
         maps_bwd[b].t[map_slot(T_G)] = maps_lse.t[map_slot(T_LSE)];
@@ -386,6 +394,9 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
         }
     }
     const int n_chunks = static_cast<int>((a->V + Vc - 1) / Vc);
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
     {
         PhaseScope ph(3, st);
         for (int j = -1; j < n_chunks; ++j) {
@@ -401,7 +412,7 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
             if (g.has_next) {
                 g.v0n = static_cast<int>((j + 1) * Vc);
                 g.vlenn = static_cast<int>(a->V - g.v0n < Vc ? a->V - g.v0n : Vc);
-                const int wb = (j + 1) & 1;
+                const int wb = (j + 1) % kGBuffers;
                 g.G_wr = G + wb * gbuf;
                 g.G_wr_lo = G_lo + wb * gbuf;
             }
@@ -410,7 +421,23 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
             g.acc_dw = a->accumulate_dW ? 1 : 0;
             g.dH_acc = dHacc;
             g.acc_dh = j > 0 ? 1 : 0;
-            k_gemm<KIND_BWD><<<grid, kThreads, kGemmSmem, st>>>(maps_bwd[j < 0 ? 0 : (j & 1)], g);
+            const GemmMaps &mp = maps_bwd[j < 0 ? 0 : j % kGBuffers];
+            if (j < 0) {
+                k_gemm<KIND_BWD><<<grid, kThreads, kGemmSmem, st>>>(mp, g);
+            } else {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3(grid);
+                cfg.blockDim = dim3(kThreads);
+                cfg.dynamicSmemBytes = kGemmSmem;
+                cfg.stream = st;
+                cfg.attrs = pdl;
+                cfg.numAttrs = 1;
+                cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm<KIND_BWD>, mp, g);
+                if (e != cudaSuccess) {
+                    t_last_cuda = e;
+                    return LCE_ERR_CUDA;
+                }
+            }
             LCE_CHECK_LAUNCH();
         }
     }

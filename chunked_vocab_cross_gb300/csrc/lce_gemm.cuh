@@ -103,9 +103,12 @@ __host__ __device__ inline long long lse_partial_rows(int rows_cap, int pairs) {
 }
 
 // Tile types. KIND_LSE launches run only T_LSE; a KIND_BWD launch for vocab
-// chunk j runs the dW and dH tiles of chunk j and the G tiles of chunk j+1
-// (into the other half of a double-buffered G), which are independent of one
-// another, so one launch per chunk needs no synchronisation inside it.
+// chunk j runs the G tiles of chunk j+1 (into the next of three G buffers)
+// and the dW and dH tiles of chunk j, which are independent of one another,
+// so a launch needs no synchronisation inside it. Consecutive KIND_BWD
+// launches overlap (programmatic dependent launch): a launch's G tiles start
+// on the SMs its predecessor frees, and its dW/dH tiles wait for the
+// predecessor (which wrote G_j and the dH accumulator) to complete.
 enum Kind : int { KIND_LSE = 0, KIND_BWD = 1 };
 enum TileType : int { T_LSE = 0, T_G = 1, T_DH = 2, T_DW = 3 };
 
@@ -180,14 +183,16 @@ __device__ inline Sched make_sched(const GemmArgs &a, int nv) {
         s.kseg_dw = cdiv(nv, kBK);
         s.kseg_dh = cdiv(a.vlen, kBK);
         s.kseg_g = cdiv(a.d, kBK);
-        s.units = s.n_dw + s.n_dh + s.n_g;
+        s.units = s.n_g + s.n_dw + s.n_dh;
     }
     return s;
 }
 
 // Unit u -> [n0, n1) tiles. LSE units are (256-row block, contiguous vocab range),
 // split-major so CTAs running together share W tiles in L2; BWD units are one
-// tile each, dW first (longest K), then dH, then G, d / vocab tiles fastest.
+// tile each: first the G tiles of the next chunk, which do not depend on the
+// previous launch and so can run while its last tiles finish, then dW (long K)
+// and dH of the current chunk; d / vocab tiles fastest.
 template <int KIND>
 __device__ inline void unit_range(const Sched &s, int u, int &n0, int &n1) {
     if (KIND == KIND_LSE) {
@@ -208,23 +213,23 @@ __device__ inline TileInfo tile_info(const Sched &s, int u, int n) {
         t.mb = u % s.m_blocks;
         t.nt = n;
         t.kseg = s.kseg;
-    } else if (u < s.n_dw) {
+    } else if (u < s.n_g) {
+        t.type = T_G;
+        t.mb = u / s.nt_g;
+        t.nt = u % s.nt_g;
+        t.kseg = s.kseg_g;
+    } else if (u < s.n_g + s.n_dw) {
+        const int q = u - s.n_g;
         t.type = T_DW;
-        t.mb = u / s.nt_d;
-        t.nt = u % s.nt_d;
+        t.mb = q / s.nt_d;
+        t.nt = q % s.nt_d;
         t.kseg = s.kseg_dw;
-    } else if (u < s.n_dw + s.n_dh) {
-        const int q = u - s.n_dw;
+    } else {
+        const int q = u - s.n_g - s.n_dw;
         t.type = T_DH;
         t.mb = q / s.nt_d;
         t.nt = q % s.nt_d;
         t.kseg = s.kseg_dh;
-    } else {
-        const int q = u - s.n_dw - s.n_dh;
-        t.type = T_G;
-        t.mb = q / s.nt_g;
-        t.nt = q % s.nt_g;
-        t.kseg = s.kseg_g;
     }
     return t;
 }
@@ -378,6 +383,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int it = 0;
             bool ok = true;
+            bool dep_done = false;
             const int arow = static_cast<int>(rank) * kBM;      // this CTA's A rows within the pair tile
             const int brow = static_cast<int>(rank) * kHalfN;   // this CTA's B rows (N) within the tile
             for (int u = pair; ok && u < s.units; u += npairs) {
@@ -385,6 +391,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 unit_range<KIND>(s, u, n0, n1);
                 for (int n = n0; ok && n < n1; ++n) {
                     const TileInfo t = tile_info<KIND>(s, u, n);
+                    if (KIND == KIND_BWD && !dep_done && t.type != T_G) {
+                        // dW / dH read what the previous launch wrote
+                        griddep_wait();
+                        griddep_launch_dependents();
+                        dep_done = true;
+                    }
                     const OperandMaps &om = maps.t[map_slot(t.type)];
                     const int k_blocks = t.kseg * a.nseg;
                     for (int kbt = 0; kbt < k_blocks; ++kbt, ++it) {
@@ -407,6 +419,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         load_operands(t, a, ma, mbp, sa, sb, fb, am, bn, k0);
                     }
                 }
+            }
+            if (KIND == KIND_BWD && !dep_done) {
+                // the next launch may only start once the one before this has finished
+                griddep_wait();
+                griddep_launch_dependents();
             }
             if (!ok && rank == 0) {
                 // let the copies already issued (by both CTAs) land before the pair exits
@@ -468,6 +485,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const float inv_nv = nv > 0 ? a.grad_scale / static_cast<float>(nv) : 0.f;
         int tile = 0;
         bool ok = true;
+        bool dep_done = false;
         for (int u = pair; ok && u < s.units; u += npairs) {
             int n0, n1;
             unit_range<KIND>(s, u, n0, n1);
@@ -475,6 +493,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int grow = 0;
             for (int n = n0; n < n1; ++n, ++tile) {
                 const TileInfo t = tile_info<KIND>(s, u, n);
+                if (KIND == KIND_BWD && !dep_done && t.type != T_G) {
+                    griddep_wait();   // the dH accumulator / dW rows of the previous launch
+                    dep_done = true;
+                }
                 // compacted row (LSE/G/DH) or chunk vocab row (DW) of this thread
                 grow = t.mb * kPairM + static_cast<int>(rank) * kBM + trow;
                 // target column relative to the first column of the vocab range
