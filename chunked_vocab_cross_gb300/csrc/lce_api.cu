@@ -152,6 +152,22 @@ bool encode_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer
     return r == CUDA_SUCCESS;
 }
 
+// Map used by bulk tensor stores from the epilogue: box {32, 32} over a
+// row-major [outer][inner] array of bf16 (64-byte swizzle) or fp32 (128-byte
+// swizzle), matching the staging layout the epilogue writes.
+bool encode_store_map(CUtensorMap *m, const void *base, bool fp32, uint64_t inner, uint64_t outer) {
+    const uint64_t elt = fp32 ? 4 : 2;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * elt};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = g_encode(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                          const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          fp32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // 3-D bf16 map over the same row-major [outer][inner] array for MN-major
 // operand tiles: dims {64, outer, inner/64} with strides {row, 128 bytes}, so
 // one box {64, box_rows, box_blocks} lands as box_blocks consecutive
@@ -393,6 +409,17 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
             return LCE_ERR_CUDA;
         }
     }
+    CUtensorMap st_g[kGBuffers][2], st_dw, st_dh;
+    for (int b = 0; b < kGBuffers; ++b)
+        if (!encode_store_map(&st_g[b][0], G + b * gbuf, false, Vc, L.N_pad) ||
+            !encode_store_map(&st_g[b][1], G_lo + b * gbuf, false, Vc, L.N_pad))
+            return LCE_ERR_CUDA;
+    if (!encode_store_map(&st_dw, a->dW, true, d, V) || !encode_store_map(&st_dh, dHacc, true, d, L.N_pad))
+        return LCE_ERR_CUDA;
+    for (int b = 0; b < kGBuffers; ++b) {
+        maps_bwd[b].st_dw = st_dw;
+        maps_bwd[b].st_dh = st_dh;
+    }
     const int n_chunks = static_cast<int>((a->V + Vc - 1) / Vc);
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -421,7 +448,11 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
             g.acc_dw = a->accumulate_dW ? 1 : 0;
             g.dH_acc = dHacc;
             g.acc_dh = j > 0 ? 1 : 0;
-            const GemmMaps &mp = maps_bwd[j < 0 ? 0 : j % kGBuffers];
+            GemmMaps mp = maps_bwd[j < 0 ? 0 : j % kGBuffers];
+            if (g.has_next) {
+                mp.st_g[0] = st_g[(j + 1) % kGBuffers][0];
+                mp.st_g[1] = st_g[(j + 1) % kGBuffers][1];
+            }
             if (j < 0) {
                 k_gemm<KIND_BWD><<<grid, kThreads, kGemmSmem, st>>>(mp, g);
             } else {

@@ -60,7 +60,12 @@ constexpr int kStageA = kBM * 128;      // this CTA's 128 A rows x 64 k
 constexpr int kStageB = kHalfN * 128;   // this CTA's 128 B rows x 64 k
 constexpr int kStageBytes = kStageA + kStageB;
 constexpr int kPairTx = 2 * kStageBytes;   // bytes both CTAs land on the even CTA's full barrier
-constexpr int kGemmSmem = kStages * kStageBytes + 1024 /*alignment slack*/ + 256 /*barriers*/;
+// Epilogue staging: each of the 4 epilogue warps owns two 4 KB buffers; a
+// 32-row x 32-column chunk (fp32, or bf16 hi + lo) is written there in the
+// TMA swizzle pattern and stored to global memory by one bulk tensor store.
+constexpr int kEpiBufBytes = 4096;
+constexpr int kEpiBytes = 4 * 2 * kEpiBufBytes;
+constexpr int kGemmSmem = kStages * kStageBytes + kEpiBytes + 1024 /*alignment slack*/ + 256 /*barriers*/;
 constexpr long long kWaitCycles = 2000000000LL;   // ~1 s: far above any legitimate wait
 constexpr long long kDrainCycles = 200000000LL;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -121,6 +126,11 @@ struct OperandMaps {
 };
 struct GemmMaps {
     OperandMaps t[3];
+    // bulk-store maps (box 32 x 32): G chunk being written (hi, lo; bf16,
+    // 64-byte swizzle), dW and the dH accumulator (fp32, 128-byte swizzle)
+    CUtensorMap st_g[2];
+    CUtensorMap st_dw;
+    CUtensorMap st_dh;
 };
 
 __host__ __device__ constexpr int map_slot(int type) { return type == T_DH ? 1 : (type == T_DW ? 2 : 0); }
@@ -329,7 +339,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);   // used on the even CTA
+    uint8_t *epi_stage = smem + kStages * kStageBytes;                            // epilogue staging buffers
+    uint64_t *full = reinterpret_cast<uint64_t *>(epi_stage + kEpiBytes);          // used on the even CTA
     uint64_t *empty = full + kStages;
     uint64_t *tfull = empty + kStages;
     uint64_t *tempty = tfull + 2;                                                   // used on the even CTA
@@ -482,6 +493,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ epilogue
         const int quarter = warp & 3;
         const int trow = quarter * 32 + lane;     // row within this CTA's 128 rows == TMEM lane
+        uint8_t *stage_mine = epi_stage + (warp - 2) * 2 * kEpiBufBytes;   // this warp's two staging buffers
+        int ebuf = 0;
         const float inv_nv = nv > 0 ? a.grad_scale / static_cast<float>(nv) : 0.f;
         int tile = 0;
         bool ok = true;
@@ -545,62 +558,73 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             run_l = run_l * exp2f(run_m - mn) + sum;
                             run_m = mn;
                         }
-                    } else if (t.type == T_G) {
-                        const size_t off = static_cast<size_t>(grow) * a.ldg + col;
-                        float g[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            float v = exp2f(__uint_as_float(r[j]) * kLog2e - lse2) * inv_nv;
-                            if (col + j == tgt) v -= inv_nv;
-                            g[j] = (col + j < a.vlenn) ? v : 0.f;
-                        }
-                        if (a.nseg == 1) {
-                            store_bf16x32(a.G_wr + off, g);
-                        } else {
-                            float lo[32];
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) split_bf16(g[j], g[j], lo[j]);
-                            store_bf16x32(a.G_wr + off, g);
-                            store_bf16x32(a.G_wr_lo + off, lo);
-                        }
                     } else {
-                        // DW: row = chunk vocab row, out = dW[v0 + row]; DH: row = compacted token
-                        const bool is_dw = t.type == T_DW;
-                        const bool row_ok = is_dw ? (grow < a.vlen) : (grow < nv);
-                        if (row_ok && col < a.d) {
-                            float *out = is_dw ? a.dW + static_cast<size_t>(a.v0 + grow) * a.d + col
-                                               : a.dH_acc + static_cast<size_t>(grow) * a.d + col;
-                            const bool accumulate = is_dw ? a.acc_dw : a.acc_dh;
-                            const bool zero_acc = (t.kseg == 0);
-                            if (col + 32 <= a.d) {
-                                float4 *o4 = reinterpret_cast<float4 *>(out);
+                        // G, DW, DH: values for this thread's row -> swizzled staging
+                        // buffer -> one bulk tensor store (or add) of the 32x32 chunk
+                        float v[32];
+                        if (t.type == T_G) {
 #pragma unroll
-                                for (int q = 0; q < 8; ++q) {
-                                    float4 v = zero_acc ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                                        : make_float4(__uint_as_float(r[4 * q]),
-                                                                      __uint_as_float(r[4 * q + 1]),
-                                                                      __uint_as_float(r[4 * q + 2]),
-                                                                      __uint_as_float(r[4 * q + 3]));
-                                    if (accumulate) {
-                                        const float4 o = o4[q];
-                                        v.x += o.x;
-                                        v.y += o.y;
-                                        v.z += o.z;
-                                        v.w += o.w;
-                                    }
-                                    o4[q] = v;
-                                }
-                            } else {
-#pragma unroll
-                                for (int j = 0; j < 32; ++j) {
-                                    if (col + j < a.d) {
-                                        float v = zero_acc ? 0.f : __uint_as_float(r[j]);
-                                        if (accumulate) v += out[j];
-                                        out[j] = v;
-                                    }
-                                }
+                            for (int j = 0; j < 32; ++j) {
+                                float g = exp2f(__uint_as_float(r[j]) * kLog2e - lse2) * inv_nv;
+                                if (col + j == tgt) g -= inv_nv;
+                                v[j] = (col + j < a.vlenn) ? g : 0.f;
                             }
+                        } else {
+                            const bool zero_acc = (t.kseg == 0);   // dW with no valid token
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = zero_acc ? 0.f : __uint_as_float(r[j]);
                         }
+                        uint8_t *sbuf = stage_mine + ebuf * kEpiBufBytes;
+                        if (lane == 0) bulk_wait_group_read<1>();   // this buffer's store of two chunks ago has read it
+                        __syncwarp();
+                        if (t.type == T_G) {
+                            // bf16 rows of 64 bytes; 16-byte unit k of row `lane` at unit k ^ ((lane >> 1) & 3)
+                            float lo[32];
+                            if (a.nseg > 1) {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) split_bf16(v[j], v[j], lo[j]);
+                            }
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const int off = lane * 64 + ((k ^ ((lane >> 1) & 3)) << 4);
+                                *reinterpret_cast<uint4 *>(sbuf + off) =
+                                    make_uint4(pack_bf16x2(v[8 * k], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
+                                               pack_bf16x2(v[8 * k + 4], v[8 * k + 5]),
+                                               pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
+                                if (a.nseg > 1)
+                                    *reinterpret_cast<uint4 *>(sbuf + 2048 + off) = make_uint4(
+                                        pack_bf16x2(lo[8 * k], lo[8 * k + 1]), pack_bf16x2(lo[8 * k + 2], lo[8 * k + 3]),
+                                        pack_bf16x2(lo[8 * k + 4], lo[8 * k + 5]), pack_bf16x2(lo[8 * k + 6], lo[8 * k + 7]));
+                            }
+                        } else {
+                            // fp32 rows of 128 bytes; 16-byte unit k of row `lane` at unit k ^ (lane & 7)
+#pragma unroll
+                            for (int k = 0; k < 8; ++k)
+                                *reinterpret_cast<float4 *>(sbuf + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                                    make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            const int row0 = t.mb * kPairM + static_cast<int>(rank) * kBM + quarter * 32;
+                            if (t.type == T_G) {
+                                tma_store_2d(&maps.st_g[0], sbuf, col, row0);
+                                if (a.nseg > 1) tma_store_2d(&maps.st_g[1], sbuf + 2048, col, row0);
+                            } else if (t.type == T_DW) {
+                                // rows past V (last chunk) are clipped by the map
+                                if (a.acc_dw)
+                                    tma_reduce_add_2d(&maps.st_dw, sbuf, col, a.v0 + row0);
+                                else
+                                    tma_store_2d(&maps.st_dw, sbuf, col, a.v0 + row0);
+                            } else {
+                                if (a.acc_dh)
+                                    tma_reduce_add_2d(&maps.st_dh, sbuf, col, row0);
+                                else
+                                    tma_store_2d(&maps.st_dh, sbuf, col, row0);
+                            }
+                            bulk_commit_group();
+                        }
+                        ebuf ^= 1;
                     }
                 }
                 tc_fence_before();
@@ -612,6 +636,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 a.part[static_cast<size_t>(split) * s.m_blocks * kPairM + grow] = make_float2(run_m, run_l);
             }
         }
+        if (lane == 0) bulk_wait_group_all();   // this warp's stores have written global memory
     }
 
     // Both CTAs stay resident until every remote arrive, multicast commit and
