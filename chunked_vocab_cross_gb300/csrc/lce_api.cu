@@ -428,7 +428,6 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
         PhaseScope ph(3, st);
         for (int j = -1; j < n_chunks; ++j) {
             GemmArgs g = ga;
-            g.ldg = static_cast<int>(Vc);
             g.lse2 = lse2;
             g.has_cur = j >= 0;
             g.has_next = j + 1 < n_chunks;

@@ -140,7 +140,6 @@ struct GemmArgs {
     int d, V;
     int num_pairs;         // CTA pairs in the grid (gridDim.x / 2)
     int nseg;              // 1 (bf16 operands) or 3 (split-precision fp32 operands)
-    int ldg;               // row stride of G in elements
     const int *tc;         // compacted targets, -1 where none
     // KIND_LSE
     float *z;              // per compacted row: target logit
@@ -149,8 +148,6 @@ struct GemmArgs {
     // G tiles of the next chunk [v0n, v0n+vlenn) (if has_next)
     int v0, vlen, v0n, vlenn, has_cur, has_next;
     const float *lse2;     // per compacted row: lse / ln 2
-    __nv_bfloat16 *G_wr;   // next chunk's G [rows][ldg], hi part
-    __nv_bfloat16 *G_wr_lo;   // lo part when nseg == 3
     float *dW;             // [V][d]
     int acc_dw;            // add into dW instead of overwriting
     float *dH_acc;         // [rows][d] fp32
@@ -279,14 +276,6 @@ __device__ __forceinline__ void split_bf16(float x, float &hi, float &lo) {
     const float h = __bfloat162float(__float2bfloat16_rn(x));
     lo = x - h;
     hi = h;
-}
-
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const float (&g)[32]) {
-    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        d4[q] = make_uint4(pack_bf16x2(g[8 * q + 0], g[8 * q + 1]), pack_bf16x2(g[8 * q + 2], g[8 * q + 3]),
-                           pack_bf16x2(g[8 * q + 4], g[8 * q + 5]), pack_bf16x2(g[8 * q + 6], g[8 * q + 7]));
 }
 
 // Issue this CTA's TMA loads of one k-block (A rows am.., B rows bn.., k0..)
