@@ -438,9 +438,6 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
             if (g.has_next) {
                 g.v0n = static_cast<int>((j + 1) * Vc);
                 g.vlenn = static_cast<int>(a->V - g.v0n < Vc ? a->V - g.v0n : Vc);
-                const int wb = (j + 1) % kGBuffers;
-                g.G_wr = G + wb * gbuf;
-                g.G_wr_lo = G_lo + wb * gbuf;
             }
             g.mn3d = 1 | (mn3d_d ? 6 : 0);
             g.dW = a->dW;
