@@ -28,6 +28,23 @@ sys.path.insert(0, ROOT)
 METRIC = "fused linear-CE fwd+bwd valid tokens/sec; % of dense BF16 tensor peak"
 UNIT = "valid tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM bytes (read + write) per backward k_gemm launch of the llama8b shape,
+# from profiles/k_gemm_pair_llama8b_v16k_ncu_full.md; valid only for the
+# kernel sources it was captured from (sha256 prefix below), else reported null.
+NCU_TRAFFIC = {"workload": "llama8b", "kernel": "backward", "bytes_per_launch": 846.0e6,
+               "src_sha256": "5951da1fc5c00685"}
+
+
+def kernel_src_sha256() -> str:
+    import glob
+    import hashlib
+    files = sorted(glob.glob(os.path.join(ROOT, "chunked_vocab_cross_gb300", "csrc", "*.cu")) +
+                   glob.glob(os.path.join(ROOT, "chunked_vocab_cross_gb300", "csrc", "*.cuh")))
+    h = hashlib.sha256()
+    for f in files:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
 
 
 def load_peaks():
@@ -301,6 +318,10 @@ def main():
     per_launch_ms = ph["ms"] / max(1, ph["launches"])
     flops_launch = gemm_flops[name] / max(1, ph["launches"] // prof_steps)
     achieved = flops_launch / (per_launch_ms / 1e3) / 1e12
+    traffic = None
+    if (NCU_TRAFFIC["workload"] == w.name and NCU_TRAFFIC["kernel"] == name and w.V == 128256
+            and NCU_TRAFFIC["src_sha256"] == kernel_src_sha256() and not args.vocab_chunk):
+        traffic = NCU_TRAFFIC["bytes_per_launch"]
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     total_prof = sum(p["ms"] for p in phases.values())
     cpu = None
@@ -321,7 +342,7 @@ def main():
             "of_sustained": tflops_useful / peak, "peaks": peak_src,
             "note": "useful FLOPs = 6*Nv*d*V; the path executes 8*Nv*d*V (logits recomputed in backward)"},
         "roofline": {"bound": "tensor", "kernel": f"k_gemm ({name})", "achieved": achieved, "peak": peak,
-                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                      "peak_kind": f"bf16_tflops_sustained ({peak_src})",
                      "flops_per_launch": flops_launch, "ms_per_launch": per_launch_ms},
         "phases_ms_per_step": {k: v["ms"] / prof_steps for k, v in phases.items()},
