@@ -31,6 +31,8 @@ SIGNATURES = {
                                     c_void_p]),
     "lce_compact": (c_int, [c_void_p, c_int64, c_int64, c_int64, c_void_p, c_void_p, c_void_p, c_void_p]),
     "lce_run": (c_int, [c_void_p]),
+    "lce_backward": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int64, c_void_p, c_void_p,
+                             c_void_p, c_void_p, c_void_p]),
     "lce_workspace_size": (c_size_t, [c_int64, c_int64, c_int64, c_int, c_int64]),
     "lce_get_device_status": (c_int, [c_void_p, ctypes.POINTER(c_int32)]),
     "lce_status_string": (ctypes.c_char_p, [c_int]),
@@ -54,6 +56,8 @@ class LceArgs(ctypes.Structure):
         ("workspace", c_void_p), ("workspace_bytes", c_size_t),
         ("vocab_chunk", c_int64),
         ("stream", c_void_p),
+        ("lse_in", c_void_p),
+        ("grad_loss", c_void_p),
     ]
 
 

@@ -245,8 +245,9 @@ int64_t pick_chunk(int64_t V, int64_t requested) {
 lce_status_t check_args(const lce_args_t *a) {
     if (!a) return LCE_ERR_NULL;
     if (a->dtype != LCE_BF16 && a->dtype != LCE_FP32) return LCE_ERR_DTYPE;
-    if (!a->H || !a->W || !a->targets || !a->loss) return LCE_ERR_NULL;
+    if (!a->H || !a->W || !a->targets) return LCE_ERR_NULL;
     if ((a->dH == nullptr) != (a->dW == nullptr)) return LCE_ERR_NULL;
+    if (a->lse_in ? !a->dH : !a->loss) return LCE_ERR_NULL;   // backward-only needs grads; forward needs loss
     if (a->N < 1 || a->N >= (int64_t(1) << 31) || a->d < 1 || a->d > 65536 || a->V < 1 ||
         a->V >= (int64_t(1) << 31))
         return LCE_ERR_SHAPE;
@@ -341,6 +342,7 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
     ga.nseg = split ? 3 : 1;
     ga.tc = tc;
     ga.grad_scale = a->grad_scale == 0.f ? 1.f : a->grad_scale;
+    ga.grad_ptr = a->grad_loss;
     const int n_tiles_v = cdiv(V, kBN);
 
     {
@@ -357,15 +359,20 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
             LCE_CHECK_LAUNCH();
         }
     }
-    {
-        PhaseScope ph(1, st);
-        GemmArgs g = ga;
-        g.z = z;
-        g.part = part;
-        k_gemm<KIND_LSE><<<grid, kThreads, kGemmSmem, st>>>(maps_lse, g);
+    if (a->lse_in) {
+        // backward from a stored lse: no forward pass
+        PhaseScope ph(2, st);
+        k_lse_from_input<<<static_cast<int>(L.N_pad / 256 + 1), 256, 0, st>>>(a->lse_in, idx, counters, lse2);
         LCE_CHECK_LAUNCH();
-    }
-    {
+    } else {
+        {
+            PhaseScope ph(1, st);
+            GemmArgs g = ga;
+            g.z = z;
+            g.part = part;
+            k_gemm<KIND_LSE><<<grid, kThreads, kGemmSmem, st>>>(maps_lse, g);
+            LCE_CHECK_LAUNCH();
+        }
         PhaseScope ph(2, st);
         k_lse_merge<<<static_cast<int>(L.N_pad / 256 + 1), 256, 0, st>>>(part, counters, n_tiles_v, pairs, z, lse2,
                                                                          loss_rows, idx, a->lse);
@@ -563,6 +570,27 @@ lce_status_t lce_forward_backward(const void *H, const void *W, const int64_t *t
     a.loss = loss;
     a.dH = dH;
     a.dW = dW;
+    a.stream = stream;
+    return lce_run(&a);
+}
+
+lce_status_t lce_backward(const void *H, const void *W, const int64_t *targets, int64_t ignore_index, int64_t N,
+                          int64_t d, int64_t V, const float *lse, const float *grad_loss, void *dH, float *dW,
+                          lce_stream_t stream) {
+    if (!lse || !dH || !dW) return LCE_ERR_NULL;
+    lce_args_t a{};
+    a.dtype = LCE_BF16;
+    a.H = H;
+    a.W = W;
+    a.targets = targets;
+    a.ignore_index = ignore_index;
+    a.N = N;
+    a.d = d;
+    a.V = V;
+    a.dH = dH;
+    a.dW = dW;
+    a.lse_in = lse;
+    a.grad_loss = grad_loss;
     a.stream = stream;
     return lce_run(&a);
 }

@@ -153,6 +153,7 @@ struct GemmArgs {
     float *dH_acc;         // [rows][d] fp32
     int acc_dh;            // add into dHacc (every chunk after the first)
     float grad_scale;      // multiplies G
+    const float *grad_ptr; // optional device scalar that also multiplies G
     // MN-major operand maps that are 3-D ({64 within a 128-byte line, K rows,
     // 64-wide column blocks}: one box per operand per stage) instead of 2-D
     // (one {64, 64} box per column block); 3-D needs the MN extent to be a
@@ -484,7 +485,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int trow = quarter * 32 + lane;     // row within this CTA's 128 rows == TMEM lane
         uint8_t *stage_mine = epi_stage + (warp - 2) * 2 * kEpiBufBytes;   // this warp's two staging buffers
         int ebuf = 0;
-        const float inv_nv = nv > 0 ? a.grad_scale / static_cast<float>(nv) : 0.f;
+        const float gscale = a.grad_ptr ? a.grad_scale * *a.grad_ptr : a.grad_scale;
+        const float inv_nv = nv > 0 ? gscale / static_cast<float>(nv) : 0.f;
         int tile = 0;
         bool ok = true;
         bool dep_done = false;

@@ -151,6 +151,16 @@ __global__ void __launch_bounds__(256)
     if (lse_user) lse_user[idx[row]] = lse;
 }
 
+// Backward from a stored lse: lse2[r] = lse_in[idx[r]] / ln 2 for the
+// compacted rows (the form the G epilogue uses).
+__global__ void __launch_bounds__(256)
+    k_lse_from_input(const float *__restrict__ lse_in, const int *__restrict__ idx, const int *__restrict__ counters,
+                     float *__restrict__ lse2_out) {
+    const int nv = counters[0];
+    const int row = blockIdx.x * blockDim.x + threadIdx.x;
+    if (row < nv) lse2_out[row] = lse_in[idx[row]] * kLog2e;
+}
+
 // loss = (sum_i loss_i) / Nv with a fixed summation tree (one CTA), so the
 // result does not depend on scheduling. Nv = 0 gives 0/0 = NaN.
 __global__ void __launch_bounds__(1024)

@@ -36,7 +36,8 @@ def workspace_size(N: int, d: int, V: int, dtype=torch.bfloat16, vocab_chunk: in
 
 
 def lce_run(H, W, targets, ignore_index: int = -100, *, loss=None, dH=None, dW=None, accumulate_dW: bool = False,
-            grad_scale: float = 1.0, lse=None, workspace=None, vocab_chunk: int = 0, stream=None) -> None:
+            grad_scale: float = 1.0, lse=None, workspace=None, vocab_chunk: int = 0, lse_in=None, grad_loss=None,
+            stream=None) -> None:
     """Raw lce_run over caller-provided output tensors."""
     _check_inputs(H, W, targets)
     a = _abi.LceArgs()
@@ -45,7 +46,9 @@ def lce_run(H, W, targets, ignore_index: int = -100, *, loss=None, dH=None, dW=N
     a.ignore_index = int(ignore_index)
     a.N, a.d = H.shape
     a.V = W.shape[0]
-    a.loss = loss.data_ptr()
+    a.loss = loss.data_ptr() if loss is not None else None
+    a.lse_in = lse_in.data_ptr() if lse_in is not None else None
+    a.grad_loss = grad_loss.data_ptr() if grad_loss is not None else None
     a.dH = dH.data_ptr() if dH is not None else None
     a.dW = dW.data_ptr() if dW is not None else None
     a.accumulate_dW = 1 if accumulate_dW else 0
@@ -99,6 +102,31 @@ def lce_forward_backward(H, W, targets, ignore_index: int = -100, *, dW=None, ac
                 grad_scale=grad_scale, lse=lse, workspace=workspace, vocab_chunk=vocab_chunk, stream=stream)
     out = (loss, dH, dW)
     return out + (lse,) if return_lse else out
+
+
+def lce_backward(H, W, targets, lse, ignore_index: int = -100, *, grad_loss=None, dW=None,
+                 accumulate_dW: bool = False, vocab_chunk: int = 0, workspace=None, stream=None):
+    """dH and dW from a stored per-row lse (lce_forward(..., return_lse=True)),
+    times the device scalar grad_loss (None = 1). Logits are recomputed."""
+    _check_inputs(H, W, targets)
+    if lse.dtype != torch.float32 or lse.shape != (H.shape[0],) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [N] tensor")
+    if grad_loss is not None:
+        grad_loss = grad_loss.detach().to(device=H.device, dtype=torch.float32).contiguous()
+    dH = torch.empty_like(H)
+    if dW is None:
+        dW = torch.empty(W.shape, dtype=torch.float32, device=W.device)
+        accumulate_dW = False
+    if (H.dtype == torch.bfloat16 and not accumulate_dW and vocab_chunk == 0 and workspace is None):
+        _abi.check(_abi.lib().lce_backward(H.data_ptr(), W.data_ptr(), targets.data_ptr(), int(ignore_index),
+                                           H.shape[0], H.shape[1], W.shape[0], lse.data_ptr(),
+                                           grad_loss.data_ptr() if grad_loss is not None else None,
+                                           dH.data_ptr(), dW.data_ptr(), _stream(stream)),
+                   "lce_backward")
+    else:
+        lce_run(H, W, targets, ignore_index, dH=dH, dW=dW, accumulate_dW=accumulate_dW, lse_in=lse,
+                grad_loss=grad_loss, vocab_chunk=vocab_chunk, workspace=workspace, stream=stream)
+    return dH, dW
 
 
 def lce_compact(targets, ignore_index: int = -100, V: int | None = None, *, stream=None):
@@ -164,6 +192,35 @@ class _LinearCrossEntropy(torch.autograd.Function):
         return gH, gW, None, None
 
 
-def linear_cross_entropy(H, W, targets, ignore_index: int = -100):
-    """loss = cross_entropy(H @ W^T, targets, ignore_index) without materialising logits."""
-    return _LinearCrossEntropy.apply(H, W, targets, ignore_index)
+class _LinearCrossEntropySplit(torch.autograd.Function):
+    """Two-call form: the forward computes the loss and keeps only the per-row
+    lse [N]; the backward recomputes the logits and applies the incoming
+    gradient on the device."""
+
+    @staticmethod
+    def forward(ctx, H, W, targets, ignore_index):
+        H, W, targets = H.contiguous(), W.contiguous(), targets.contiguous()
+        loss, lse = lce_forward(H, W, targets, ignore_index, return_lse=True)
+        ctx.save_for_backward(H, W, targets, lse)
+        ctx.ignore_index = ignore_index
+        return loss
+
+    @staticmethod
+    def backward(ctx, g):
+        H, W, targets, lse = ctx.saved_tensors
+        dH, dW = lce_backward(H, W, targets, lse, ctx.ignore_index, grad_loss=g)
+        return (dH if ctx.needs_input_grad[0] else None,
+                dW.to(W.dtype) if ctx.needs_input_grad[1] else None, None, None)
+
+
+def linear_cross_entropy(H, W, targets, ignore_index: int = -100, fused: bool = True):
+    """loss = cross_entropy(H @ W^T, targets, ignore_index) without materialising logits.
+
+    fused=True computes dH and dW during the forward call and keeps them until
+    backward (for a forward that is always followed by backward). fused=False
+    keeps only the per-row lse [N] in forward and runs the gradient passes in
+    backward with the incoming gradient applied on the device: the same total
+    work, split across the two calls, and a forward without gradient work."""
+    if fused:
+        return _LinearCrossEntropy.apply(H, W, targets, ignore_index)
+    return _LinearCrossEntropySplit.apply(H, W, targets, ignore_index)

@@ -131,10 +131,29 @@ typedef struct {
     size_t workspace_bytes;   /* size of `workspace` */
     int64_t vocab_chunk;      /* vocab rows per backward chunk; 0 = default; else a multiple of 256 */
     lce_stream_t stream;
+    const float *lse_in;      /* optional [N] fp32 per-row logsumexp from an earlier forward (the `lse`
+                                 output of lce_run): the forward pass is skipped, only dH/dW are
+                                 computed (dH and dW required, loss may be NULL) */
+    const float *grad_loss;   /* optional device fp32 scalar: upstream gradient of the loss,
+                                 multiplies dH and dW (read on the device, no host sync) */
 } lce_args_t;
 
-/* Forward, or forward + backward when dH/dW are given, with every option. */
+/* Forward, or forward + backward when dH/dW are given, or backward alone
+ * from a stored lse (lse_in), with every option. */
 lce_status_t lce_run(const lce_args_t *args);
+
+/*
+ * Backward alone, for a training loop that runs the forward and backward
+ * passes at different times: dH [N,d] bf16 and dW [V,d] fp32 (overwritten)
+ * from the per-row lse [N] fp32 that a forward stored (lce_run with
+ * args.lse), times the device scalar *grad_loss (NULL = 1). The logits are
+ * recomputed from H and W ("6GB显卡预训练11亿参数模型", section "关键参数说明":
+ * the chunked loss recomputes logits in backward instead of keeping them).
+ * H, W, targets and ignore_index must be those of the forward.
+ */
+lce_status_t lce_backward(const void *H, const void *W, const int64_t *targets, int64_t ignore_index,
+                          int64_t N, int64_t d, int64_t V, const float *lse, const float *grad_loss,
+                          void *dH, float *dW, lce_stream_t stream);
 
 /*
  * Bytes of scratch lce_run needs for these sizes (what the library allocates

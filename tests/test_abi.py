@@ -28,7 +28,7 @@ def _declared():
 
 def test_header_declares_expected_entry_points():
     names = _declared()
-    for n in ("lce_forward", "lce_forward_backward", "lce_run", "lce_workspace_size", "lce_compact",
+    for n in ("lce_forward", "lce_forward_backward", "lce_backward", "lce_run", "lce_workspace_size", "lce_compact",
               "lce_get_device_status", "lce_status_string"):
         assert n in names
 
@@ -83,6 +83,7 @@ int main(void) {{
 #define F(x) printf(" %zu", offsetof(lce_args_t, x));
   F(dtype) F(H) F(W) F(targets) F(ignore_index) F(N) F(d) F(V) F(loss) F(dH) F(dW)
   F(accumulate_dW) F(grad_scale) F(lse) F(workspace) F(workspace_bytes) F(vocab_chunk) F(stream)
+  F(lse_in) F(grad_loss)
   printf("\\n"); return 0; }}
 """
     with tempfile.TemporaryDirectory() as d:

@@ -230,3 +230,40 @@ def test_caller_workspace_and_size():
     small = torch.empty(n - 256, dtype=torch.uint8, device="cuda")
     with pytest.raises(lce.LceError):
         lce.lce_forward_backward(H, W, t, IGNORE_INDEX, workspace=small)
+
+
+# ------------------------------------------------ backward from a stored lse
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_backward_from_stored_lse(dtype):
+    """Forward keeps the per-row lse; a separate backward call recomputes the
+    logits and produces dH and dW, scaled by a device-side upstream gradient."""
+    base = "gpt1b" if dtype == "bf16" else "tiny"
+    x = make_inputs(base, N=900, d=256, V=5000, padding=("random_frac", 0.25), seqs=1)
+    H, W, t = to_device(x)
+    loss, lse = lce.lce_forward(H, W, t, IGNORE_INDEX, return_lse=True)
+    g = torch.tensor(2.5, device="cuda")
+    dH, dW = lce.lce_backward(H, W, t, lse, IGNORE_INDEX, grad_loss=g)
+    torch.cuda.synchronize()
+    assert lce.device_status() == 0
+    ref = oracle.forward_backward(x.H_f32(), x.W_f32(), x.targets, IGNORE_INDEX)
+    assert abs(loss.item() - ref["loss"]) <= TOL_LOSS
+    assert rel_fro(np64(dH), 2.5 * ref["dH"]) <= TOL_REL
+    assert rel_fro(np64(dW), 2.5 * ref["dW"]) <= TOL_REL
+    # same as the fused call up to the rounding of the stored lse
+    _, dH2, dW2 = lce.lce_forward_backward(H, W, t, IGNORE_INDEX, grad_scale=2.5)
+    assert rel_fro(np64(dW), np64(dW2)) <= 1e-4
+    assert rel_fro(np64(dH), np64(dH2)) <= 1e-2      # dH is rounded to bf16 / exact fp32
+
+
+def test_autograd_split_form():
+    x = make_inputs("gpt1b", N=300, d=128, V=2100, padding=("random_frac", 0.1), seqs=1)
+    H, W, t = to_device(x)
+    H.requires_grad_(True)
+    W.requires_grad_(True)
+    loss = lce.linear_cross_entropy(H, W, t, IGNORE_INDEX, fused=False)
+    (3.0 * loss).backward()
+    ref = oracle.forward_backward(x.H_f32(), x.W_f32(), x.targets, IGNORE_INDEX)
+    assert abs(loss.item() - ref["loss"]) <= TOL_LOSS
+    assert rel_fro(np64(H.grad), 3 * ref["dH"]) <= 1e-2
+    assert rel_fro(np64(W.grad), 3 * ref["dW"]) <= 1e-2
