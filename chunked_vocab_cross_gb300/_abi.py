@@ -34,6 +34,7 @@ SIGNATURES = {
     "lce_backward": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int64, c_void_p, c_void_p,
                              c_void_p, c_void_p, c_void_p]),
     "lce_workspace_size": (c_size_t, [c_int64, c_int64, c_int64, c_int, c_int64]),
+    "lce_workspace_size_args": (c_size_t, [c_void_p]),
     "lce_get_device_status": (c_int, [c_void_p, ctypes.POINTER(c_int32)]),
     "lce_status_string": (ctypes.c_char_p, [c_int]),
     "lce_last_cuda_error": (c_int, []),
@@ -58,6 +59,7 @@ class LceArgs(ctypes.Structure):
         ("stream", c_void_p),
         ("lse_in", c_void_p),
         ("grad_loss", c_void_p),
+        ("token_chunk", c_int64),
     ]
 
 

@@ -7,7 +7,7 @@
 //   2 k_gather         Hc = H[idx], zero-padded to 128-row blocks
 //   3 k_gemm<LSE>      logits tiles + online log-sum-exp partials + target logit
 //   4 k_lse_merge      lse per row, loss_i
-//   5 k_loss_reduce    loss = mean loss_i
+//   5 k_loss_partial   sum of loss_i (k_loss_final: loss = sum / Nv)
 //   backward, one launch per vocab chunk j of Vc rows (j = -1 .. chunks-1):
 //   6 k_gemm<BWD>      G_{j+1} = (softmax - onehot)/Nv from recomputed logits
 //                      of chunk j+1, dW[chunk j] = G_j^T Hc and
@@ -193,13 +193,13 @@ inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 struct Layout {
     int64_t N_pad = 0, Vc = 0, part_rows = 0;
     size_t idx = 0, inv = 0, counters = 0, tc = 0, z = 0, lse2 = 0, loss_rows = 0, part = 0, Hc = 0, Hc_lo = 0,
-           W_hi = 0, W_lo = 0, G = 0, G_lo = 0, dHacc = 0, total = 0;
+           W_hi = 0, W_lo = 0, G = 0, G_lo = 0, dHacc = 0, gcount = 0, lpart = 0, total = 0;
 };
 
 // Every operand the tensor cores read is bf16. fp32 inputs are carried as bf16
 // hi/lo pairs (Hc/Hc_lo, W_hi/W_lo, G/G_lo), so the fp32 path also holds a
 // split copy of W (4*V*d bytes).
-Layout make_layout(int64_t N, int64_t d, int64_t V, lce_dtype_t dt, int64_t Vc, bool backward) {
+Layout make_layout(int64_t N, int64_t d, int64_t V, lce_dtype_t dt, int64_t Vc, bool backward, int n_tc = 1) {
     Layout L;
     const bool split = dt == LCE_FP32;
     L.N_pad = (N + kPairM - 1) / kPairM * kPairM;
@@ -232,9 +232,14 @@ Layout make_layout(int64_t N, int64_t d, int64_t V, lce_dtype_t dt, int64_t Vc, 
         if (split) L.G_lo = take(kGBuffers * L.N_pad * Vc * 2);
         L.dHacc = take(L.N_pad * d * 4);
     }
+    L.gcount = take(64);               // valid count of the whole call (token chunks)
+    L.lpart = take(size_t(n_tc) * 8);  // per-token-chunk loss sums
     L.total = o;
     return L;
 }
+
+// Rows per token chunk: all N unless the caller capped it.
+int64_t token_rows(int64_t N, int64_t token_chunk) { return token_chunk > 0 && token_chunk < N ? token_chunk : N; }
 
 int64_t pick_chunk(int64_t V, int64_t requested) {
     const int64_t vpad = (V + kBN - 1) / kBN * kBN;
@@ -252,7 +257,7 @@ lce_status_t check_args(const lce_args_t *a) {
         a->V >= (int64_t(1) << 31))
         return LCE_ERR_SHAPE;
     if (a->vocab_chunk < 0 || (a->vocab_chunk > 0 && (a->vocab_chunk % kBN) != 0) ||
-        a->vocab_chunk > (int64_t(1) << 20))
+        a->vocab_chunk > (int64_t(1) << 20) || a->token_chunk < 0)
         return LCE_ERR_SHAPE;
     if (a->d % 8) return LCE_ERR_ALIGN;   // bf16 rows (operands or their split copies) of 16-byte multiples
     auto mis = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
@@ -281,29 +286,23 @@ struct WsGuard {
         }                                      \
     } while (0)
 
+// One token chunk of a call: rows [r0, r0 + a->N) of the caller's arrays
+// (a is already offset to them), normalised by *nv_norm, its loss sum into
+// *lpart, dW added into (acc_dw) or written.
+struct RowsCtx {
+    const int *nv_norm;   // nullptr: this chunk's own valid count
+    double *lpart;
+    bool acc_dw;
+    bool split_w;         // split an fp32 W into bf16 hi/lo (first chunk only)
+};
+
 template <typename T>
-lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
+lce_status_t run_rows(const lce_args_t *a, const DevInfo &di, uint8_t *base, const Layout &L, int64_t Vc,
+                      const RowsCtx &ctx) {
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(a->stream);
     const bool backward = a->dH != nullptr;
     const bool split = a->dtype == LCE_FP32;
-    const int64_t Vc = pick_chunk(a->V, a->vocab_chunk);
-    const Layout L = make_layout(a->N, a->d, a->V, a->dtype, Vc, backward);
     const int N = static_cast<int>(a->N), d = static_cast<int>(a->d), V = static_cast<int>(a->V);
-
-    WsGuard ws;
-    ws.s = st;
-    if (a->workspace) {
-        if (a->workspace_bytes < L.total) return LCE_ERR_WORKSPACE;
-        ws.p = a->workspace;
-    } else {
-        cudaError_t e = cudaMallocAsync(&ws.p, L.total, st);
-        if (e != cudaSuccess) {
-            t_last_cuda = e;
-            return LCE_ERR_CUDA;
-        }
-        ws.owned = true;
-    }
-    uint8_t *base = static_cast<uint8_t *>(ws.p);
     auto bf = [&](size_t off) { return reinterpret_cast<__nv_bfloat16 *>(base + off); };
     int *idx = reinterpret_cast<int *>(base + L.idx);
     int *inv = reinterpret_cast<int *>(base + L.inv);
@@ -334,6 +333,7 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
 
     GemmArgs ga{};
     ga.counters = counters;
+    ga.nv_norm = ctx.nv_norm ? ctx.nv_norm : counters;
     ga.d = d;
     ga.V = V;
     const int pairs = di.sms / 2;          // one CTA pair per two SMs
@@ -353,7 +353,7 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
         k_gather<T><<<ggrid, 256, 0, st>>>(static_cast<const T *>(a->H), a->targets, d, a->V, idx, counters, Hc,
                                            Hc_lo, tc, z);
         LCE_CHECK_LAUNCH();
-        if (split) {
+        if (split && ctx.split_w) {
             k_split_rows<<<4 * di.sms, 256, 0, st>>>(static_cast<const float *>(a->W), static_cast<size_t>(V) * d,
                                                      bf(L.W_hi), bf(L.W_lo));
             LCE_CHECK_LAUNCH();
@@ -377,7 +377,7 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
         k_lse_merge<<<static_cast<int>(L.N_pad / 256 + 1), 256, 0, st>>>(part, counters, n_tiles_v, pairs, z, lse2,
                                                                          loss_rows, idx, a->lse);
         LCE_CHECK_LAUNCH();
-        k_loss_reduce<<<1, 1024, 0, st>>>(loss_rows, counters, a->loss);
+        k_loss_partial<<<1, 1024, 0, st>>>(loss_rows, counters, ctx.lpart);
         LCE_CHECK_LAUNCH();
     }
     if (!backward) return LCE_OK;
@@ -448,7 +448,7 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
             }
             g.mn3d = 1 | (mn3d_d ? 6 : 0);
             g.dW = a->dW;
-            g.acc_dw = a->accumulate_dW ? 1 : 0;
+            g.acc_dw = ctx.acc_dw ? 1 : 0;
             g.dH_acc = dHacc;
             g.acc_dh = j > 0 ? 1 : 0;
             GemmMaps mp = maps_bwd[j < 0 ? 0 : j % kGBuffers];
@@ -479,6 +479,65 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
         PhaseScope ph(4, st);
         const int sgrid = N < 8 * di.sms ? N : 8 * di.sms;
         k_dh_scatter<T><<<sgrid, 256, 0, st>>>(dHacc, inv, N, d, static_cast<T *>(a->dH));
+        LCE_CHECK_LAUNCH();
+    }
+    return LCE_OK;
+}
+
+template <typename T>
+lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(a->stream);
+    const bool backward = a->dH != nullptr;
+    const int64_t Vc = pick_chunk(a->V, a->vocab_chunk);
+    const int64_t C = token_rows(a->N, a->token_chunk);
+    const int n_tc = static_cast<int>((a->N + C - 1) / C);
+    const Layout L = make_layout(C, a->d, a->V, a->dtype, Vc, backward, n_tc);
+
+    WsGuard ws;
+    ws.s = st;
+    if (a->workspace) {
+        if (a->workspace_bytes < L.total) return LCE_ERR_WORKSPACE;
+        ws.p = a->workspace;
+    } else {
+        cudaError_t e = cudaMallocAsync(&ws.p, L.total, st);
+        if (e != cudaSuccess) {
+            t_last_cuda = e;
+            return LCE_ERR_CUDA;
+        }
+        ws.owned = true;
+    }
+    uint8_t *base = static_cast<uint8_t *>(ws.p);
+    int *gcount = reinterpret_cast<int *>(base + L.gcount);
+    double *lpart = reinterpret_cast<double *>(base + L.lpart);
+    const bool chunked = n_tc > 1;
+    if (chunked) {
+        // the normaliser is the valid count of all N rows, known before any chunk
+        PhaseScope ph(0, st);
+        k_count_valid<<<1, 1024, 0, st>>>(a->targets, static_cast<int>(a->N), a->ignore_index, gcount);
+        LCE_CHECK_LAUNCH();
+    }
+    const size_t elt = a->dtype == LCE_BF16 ? 2 : 4;
+    for (int c = 0; c < n_tc; ++c) {
+        const int64_t r0 = c * C;
+        lce_args_t ac = *a;
+        ac.N = (a->N - r0 < C) ? a->N - r0 : C;
+        ac.H = static_cast<const uint8_t *>(a->H) + r0 * a->d * elt;
+        ac.targets = a->targets + r0;
+        if (a->dH) ac.dH = static_cast<uint8_t *>(a->dH) + r0 * a->d * elt;
+        if (a->lse) ac.lse = a->lse + r0;
+        if (a->lse_in) ac.lse_in = a->lse_in + r0;
+        RowsCtx ctx;
+        ctx.nv_norm = chunked ? gcount : nullptr;
+        ctx.lpart = lpart + c;
+        ctx.acc_dw = a->accumulate_dW || c > 0;
+        ctx.split_w = c == 0;
+        const lce_status_t s = run_rows<T>(&ac, di, base, L, Vc, ctx);
+        if (s != LCE_OK) return s;
+    }
+    if (!a->lse_in) {
+        PhaseScope ph(2, st);
+        const int *nvn = chunked ? gcount : reinterpret_cast<const int *>(base + L.counters);
+        k_loss_final<<<1, 32, 0, st>>>(lpart, n_tc, nvn, a->loss);
         LCE_CHECK_LAUNCH();
     }
     return LCE_OK;
@@ -615,6 +674,17 @@ size_t lce_workspace_size(int64_t N, int64_t d, int64_t V, lce_dtype_t dtype, in
     if (dtype != LCE_BF16 && dtype != LCE_FP32) return 0;
     if (vocab_chunk < 0 || (vocab_chunk > 0 && vocab_chunk % kBN)) return 0;
     return make_layout(N, d, V, dtype, pick_chunk(V, vocab_chunk), true).total;
+}
+
+size_t lce_workspace_size_args(const lce_args_t *a) {
+    if (!a || a->N < 1 || a->N >= (int64_t(1) << 31) || a->d < 1 || a->d > 65536 || a->V < 1 ||
+        a->V >= (int64_t(1) << 31))
+        return 0;
+    if (a->dtype != LCE_BF16 && a->dtype != LCE_FP32) return 0;
+    if (a->vocab_chunk < 0 || (a->vocab_chunk > 0 && a->vocab_chunk % kBN) || a->token_chunk < 0) return 0;
+    const int64_t C = token_rows(a->N, a->token_chunk);
+    const int n_tc = static_cast<int>((a->N + C - 1) / C);
+    return make_layout(C, a->d, a->V, a->dtype, pick_chunk(a->V, a->vocab_chunk), a->dH != nullptr, n_tc).total;
 }
 
 lce_status_t lce_get_device_status(lce_stream_t stream, int32_t *bits) {

@@ -136,7 +136,8 @@ struct GemmMaps {
 __host__ __device__ constexpr int map_slot(int type) { return type == T_DH ? 1 : (type == T_DW ? 2 : 0); }
 
 struct GemmArgs {
-    const int *counters;   // counters[0] = Nv (written by the compaction kernel)
+    const int *counters;   // counters[0] = valid rows this launch tiles (written by the compaction kernel)
+    const int *nv_norm;    // *nv_norm = Nv of the whole call, the loss normaliser
     int d, V;
     int num_pairs;         // CTA pairs in the grid (gridDim.x / 2)
     int nseg;              // 1 (bf16 operands) or 3 (split-precision fp32 operands)
@@ -486,7 +487,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint8_t *stage_mine = epi_stage + (warp - 2) * 2 * kEpiBufBytes;   // this warp's two staging buffers
         int ebuf = 0;
         const float gscale = a.grad_ptr ? a.grad_scale * *a.grad_ptr : a.grad_scale;
-        const float inv_nv = nv > 0 ? gscale / static_cast<float>(nv) : 0.f;
+        const int nvn = *a.nv_norm;
+        const float inv_nv = nvn > 0 ? gscale / static_cast<float>(nvn) : 0.f;
         int tile = 0;
         bool ok = true;
         bool dep_done = false;

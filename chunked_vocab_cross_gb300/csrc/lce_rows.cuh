@@ -161,10 +161,10 @@ __global__ void __launch_bounds__(256)
     if (row < nv) lse2_out[row] = lse_in[idx[row]] * kLog2e;
 }
 
-// loss = (sum_i loss_i) / Nv with a fixed summation tree (one CTA), so the
-// result does not depend on scheduling. Nv = 0 gives 0/0 = NaN.
+// Sum of loss_i over this call's (or token chunk's) valid rows with a fixed
+// summation tree (one CTA, fp64), so the result does not depend on scheduling.
 __global__ void __launch_bounds__(1024)
-    k_loss_reduce(const float *__restrict__ loss_rows, const int *__restrict__ counters, float *__restrict__ loss) {
+    k_loss_partial(const float *__restrict__ loss_rows, const int *__restrict__ counters, double *__restrict__ out) {
     __shared__ double sh[1024];
     const int nv = counters[0];
     double acc = 0.0;
@@ -175,7 +175,33 @@ __global__ void __launch_bounds__(1024)
         if (static_cast<int>(threadIdx.x) < w) sh[threadIdx.x] += sh[threadIdx.x + w];
         __syncthreads();
     }
-    if (threadIdx.x == 0) loss[0] = static_cast<float>(sh[0] / static_cast<double>(nv));
+    if (threadIdx.x == 0) out[0] = sh[0];
+}
+
+// loss = (sum of the partial sums, in order) / Nv. Nv = 0 gives 0/0 = NaN.
+__global__ void k_loss_final(const double *__restrict__ partials, int n, const int *__restrict__ nv_norm,
+                             float *__restrict__ loss) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    double s = 0.0;
+    for (int i = 0; i < n; ++i) s += partials[i];
+    loss[0] = static_cast<float>(s / static_cast<double>(nv_norm[0]));
+}
+
+// Number of valid (non-ignored) targets over all N positions, for the
+// normaliser when the rows are processed in token chunks.
+__global__ void __launch_bounds__(1024)
+    k_count_valid(const int64_t *__restrict__ t, int N, int64_t ignore_index, int *__restrict__ count) {
+    __shared__ int sh[32];
+    int c = 0;
+    for (int i = threadIdx.x; i < N; i += 1024) c += t[i] != ignore_index ? 1 : 0;
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_down_sync(0xffffffffu, c, o);
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = c;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        c = sh[threadIdx.x];
+        for (int o = 16; o > 0; o >>= 1) c += __shfl_down_sync(0xffffffffu, c, o);
+        if (threadIdx.x == 0) count[0] = c;
+    }
 }
 
 __device__ __forceinline__ void store_row_elems(__nv_bfloat16 *dst, const float4 a, const float4 b) {

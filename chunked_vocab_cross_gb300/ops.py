@@ -31,13 +31,19 @@ def _check_inputs(H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor):
         raise ValueError("H, W and targets must be contiguous")
 
 
-def workspace_size(N: int, d: int, V: int, dtype=torch.bfloat16, vocab_chunk: int = 0) -> int:
-    return int(_abi.lib().lce_workspace_size(N, d, V, _DT[dtype], vocab_chunk))
+def workspace_size(N: int, d: int, V: int, dtype=torch.bfloat16, vocab_chunk: int = 0, token_chunk: int = 0,
+                   backward: bool = True) -> int:
+    a = _abi.LceArgs()
+    a.dtype = _DT[dtype]
+    a.N, a.d, a.V = N, d, V
+    a.vocab_chunk, a.token_chunk = vocab_chunk, token_chunk
+    a.dH = 1 if backward else None      # only whether gradients are wanted matters
+    return int(_abi.lib().lce_workspace_size_args(ctypes.byref(a)))
 
 
 def lce_run(H, W, targets, ignore_index: int = -100, *, loss=None, dH=None, dW=None, accumulate_dW: bool = False,
             grad_scale: float = 1.0, lse=None, workspace=None, vocab_chunk: int = 0, lse_in=None, grad_loss=None,
-            stream=None) -> None:
+            token_chunk: int = 0, stream=None) -> None:
     """Raw lce_run over caller-provided output tensors."""
     _check_inputs(H, W, targets)
     a = _abi.LceArgs()
@@ -58,6 +64,7 @@ def lce_run(H, W, targets, ignore_index: int = -100, *, loss=None, dH=None, dW=N
         a.workspace = workspace.data_ptr()
         a.workspace_bytes = workspace.numel() * workspace.element_size()
     a.vocab_chunk = int(vocab_chunk)
+    a.token_chunk = int(token_chunk)
     a.stream = _stream(stream)
     _abi.check(_abi.lib().lce_run(ctypes.byref(a)), "lce_run")
 
@@ -78,7 +85,7 @@ def lce_forward(H, W, targets, ignore_index: int = -100, *, return_lse: bool = F
 
 def lce_forward_backward(H, W, targets, ignore_index: int = -100, *, dW=None, accumulate_dW: bool = False,
                          grad_scale: float = 1.0, vocab_chunk: int = 0, return_lse: bool = False,
-                         workspace=None, stream=None):
+                         workspace=None, token_chunk: int = 0, stream=None):
     """Loss, dH (H's dtype, zero on ignored rows) and dW (fp32) in one pass."""
     _check_inputs(H, W, targets)
     loss = torch.empty((), dtype=torch.float32, device=H.device)
@@ -90,7 +97,7 @@ def lce_forward_backward(H, W, targets, ignore_index: int = -100, *, dW=None, ac
         raise ValueError("dW must be a contiguous fp32 tensor shaped like W")
     lse = torch.empty(H.shape[0], dtype=torch.float32, device=H.device) if return_lse else None
     simple = (H.dtype == torch.bfloat16 and not accumulate_dW and grad_scale == 1.0 and vocab_chunk == 0
-              and not return_lse and workspace is None)
+              and not return_lse and workspace is None and token_chunk == 0)
     if simple:
         _abi.check(_abi.lib().lce_forward_backward(H.data_ptr(), W.data_ptr(), targets.data_ptr(),
                                                    int(ignore_index), H.shape[0], H.shape[1], W.shape[0],
@@ -99,7 +106,8 @@ def lce_forward_backward(H, W, targets, ignore_index: int = -100, *, dW=None, ac
                    "lce_forward_backward")
     else:
         lce_run(H, W, targets, ignore_index, loss=loss, dH=dH, dW=dW, accumulate_dW=accumulate_dW,
-                grad_scale=grad_scale, lse=lse, workspace=workspace, vocab_chunk=vocab_chunk, stream=stream)
+                grad_scale=grad_scale, lse=lse, workspace=workspace, vocab_chunk=vocab_chunk,
+                token_chunk=token_chunk, stream=stream)
     out = (loss, dH, dW)
     return out + (lse,) if return_lse else out
 

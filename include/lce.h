@@ -136,6 +136,10 @@ typedef struct {
                                  computed (dH and dW required, loss may be NULL) */
     const float *grad_loss;   /* optional device fp32 scalar: upstream gradient of the loss,
                                  multiplies dH and dW (read on the device, no host sync) */
+    int64_t token_chunk;      /* 0 = all N rows at once; else the rows are processed token_chunk
+                                 positions at a time (scratch O(token_chunk*(d + vocab_chunk)),
+                                 dW accumulated across chunks in a fixed order): the chunked loss
+                                 of "6GB显卡预训练11亿参数模型", section "关键参数说明" (--chunked-loss 512) */
 } lce_args_t;
 
 /* Forward, or forward + backward when dH/dW are given, or backward alone
@@ -161,6 +165,10 @@ lce_status_t lce_backward(const void *H, const void *W, const int64_t *targets, 
  * with N*V. Returns 0 for invalid arguments.
  */
 size_t lce_workspace_size(int64_t N, int64_t d, int64_t V, lce_dtype_t dtype, int64_t vocab_chunk);
+
+/* Bytes of scratch lce_run needs for exactly these arguments (all options,
+ * token_chunk included); 0 for invalid arguments. Pointers are not read. */
+size_t lce_workspace_size_args(const lce_args_t *args);
 
 /*
  * Synchronises `stream`, then returns in *bits the current device's status

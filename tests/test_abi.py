@@ -83,7 +83,7 @@ int main(void) {{
 #define F(x) printf(" %zu", offsetof(lce_args_t, x));
   F(dtype) F(H) F(W) F(targets) F(ignore_index) F(N) F(d) F(V) F(loss) F(dH) F(dW)
   F(accumulate_dW) F(grad_scale) F(lse) F(workspace) F(workspace_bytes) F(vocab_chunk) F(stream)
-  F(lse_in) F(grad_loss)
+  F(lse_in) F(grad_loss) F(token_chunk)
   printf("\\n"); return 0; }}
 """
     with tempfile.TemporaryDirectory() as d:

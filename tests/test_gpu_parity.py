@@ -267,3 +267,43 @@ def test_autograd_split_form():
     assert abs(loss.item() - ref["loss"]) <= TOL_LOSS
     assert rel_fro(np64(H.grad), 3 * ref["dH"]) <= 1e-2
     assert rel_fro(np64(W.grad), 3 * ref["dW"]) <= 1e-2
+
+
+# ---------------------------------------------------------- token chunk cap
+
+@pytest.mark.parametrize("token_chunk", [512, 1000])
+def test_token_chunk_cap(token_chunk):
+    """Rows processed token_chunk positions at a time: same loss and dH, dW
+    summed across chunks in a fixed order, and scratch bounded by the cap."""
+    x = make_inputs("gpt1b", N=2600, d=256, V=5000, padding=("random_frac", 0.3), seqs=1)
+    H, W, t = to_device(x)
+    loss_c, dH_c, dW_c, lse_c = lce.lce_forward_backward(H, W, t, IGNORE_INDEX, token_chunk=token_chunk,
+                                                         return_lse=True)
+    loss, dH, dW, lse = lce.lce_forward_backward(H, W, t, IGNORE_INDEX, return_lse=True)
+    torch.cuda.synchronize()
+    assert lce.device_status() == 0
+    ref = oracle.forward_backward(x.H_f32(), x.W_f32(), x.targets, IGNORE_INDEX)
+    assert abs(loss_c.item() - ref["loss"]) <= TOL_LOSS
+    assert rel_fro(np64(dH_c), ref["dH"]) <= TOL_REL
+    assert rel_fro(np64(dW_c), ref["dW"]) <= TOL_REL
+    assert abs(loss_c.item() - loss.item()) <= 1e-6
+    # the log-sum-exp merge order follows the number of row blocks per chunk,
+    # so the chunked call agrees with the whole-batch one to rounding only
+    valid = x.targets != IGNORE_INDEX
+    np.testing.assert_allclose(np64(lse_c)[valid], np64(lse)[valid], rtol=0, atol=1e-5)
+    assert rel_fro(np64(dH_c), np64(dH)) <= 1e-3
+    assert rel_fro(np64(dW_c), np64(dW)) <= 1e-4
+    assert lce.workspace_size(2600, 256, 5000, token_chunk=token_chunk) < lce.workspace_size(2600, 256, 5000)
+
+
+def test_token_chunk_backward_from_stored_lse():
+    x = make_inputs("gpt1b", N=1500, d=128, V=3000, padding=("random_frac", 0.2), seqs=1)
+    H, W, t = to_device(x)
+    loss, lse = lce.lce_forward(H, W, t, IGNORE_INDEX, return_lse=True)
+    dH = torch.empty_like(H)
+    dW = torch.empty(W.shape, dtype=torch.float32, device="cuda")
+    lce.lce_run(H, W, t, IGNORE_INDEX, dH=dH, dW=dW, lse_in=lse, token_chunk=400)
+    torch.cuda.synchronize()
+    ref = oracle.forward_backward(x.H_f32(), x.W_f32(), x.targets, IGNORE_INDEX)
+    assert rel_fro(np64(dH), ref["dH"]) <= TOL_REL
+    assert rel_fro(np64(dW), ref["dW"]) <= TOL_REL
