@@ -1,0 +1,61 @@
+"""Host-side logic of bench.py without a GPU: the multi-rank reductions with
+the gloo backend (two processes), the clock-record parsing, and that the
+reference arm's non-zero ranks exit without output."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+_WORKER = r"""
+import os, sys, json
+sys.path.insert(0, {root!r})
+import torch.distributed as dist
+import bench
+dist.init_process_group("gloo", rank=int(os.environ["RANK"]), world_size=2)
+rank = dist.get_rank()
+ms = bench.max_over_ranks(10.0 + rank, 2, device="cpu")
+tot = bench.sum_over_ranks(1000.0 * (rank + 1), 2, device="cpu")
+bench.barrier(2)
+print(json.dumps({{"rank": rank, "ms": ms, "tot": tot}}), flush=True)
+dist.destroy_process_group()
+"""
+
+
+def test_two_rank_reductions_gloo(tmp_path):
+    pytest.importorskip("torch")
+    script = tmp_path / "w.py"
+    script.write_text(_WORKER.format(root=ROOT))
+    procs = []
+    for r in range(2):
+        env = dict(os.environ, RANK=str(r), WORLD_SIZE="2", MASTER_ADDR="127.0.0.1", MASTER_PORT="29533")
+        procs.append(subprocess.Popen([sys.executable, str(script)], env=env, stdout=subprocess.PIPE,
+                                      stderr=subprocess.PIPE, text=True))
+    outs = [p.communicate(timeout=120) for p in procs]
+    for p, (o, e) in zip(procs, outs):
+        assert p.returncode == 0, e
+    res = [json.loads(o.strip().splitlines()[-1]) for o, _ in outs]
+    for r in res:
+        assert r["ms"] == 11.0          # max over ranks: the slowest rank's time
+        assert r["tot"] == 3000.0       # whole-job total
+
+
+def test_clock_summary_parsing():
+    import bench
+    c = bench.ClockSampler(0)
+    c.out = ("1800, 2070, 1350.5, Not Active, Not Active, Not Active, Active\n"
+             "1900, 2070, 1390.1, Not Active, Not Active, Not Active, Not Active\n"
+             "garbage line\n")
+    s = c.summary()
+    assert s["sm_mhz"] == 1850.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 2
+
+
+def test_reference_arm_other_ranks_exit_silently():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == ""

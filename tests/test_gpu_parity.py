@@ -307,3 +307,63 @@ def test_token_chunk_backward_from_stored_lse():
     ref = oracle.forward_backward(x.H_f32(), x.W_f32(), x.targets, IGNORE_INDEX)
     assert rel_fro(np64(dH), ref["dH"]) <= TOL_REL
     assert rel_fro(np64(dW), ref["dW"]) <= TOL_REL
+
+
+# ---------------------------------------------------------------- edge cases
+
+def _oracle_check(H, W, t, x_H, x_W, targets, ignore_index=IGNORE_INDEX, **kw):
+    loss, dH, dW = lce.lce_forward_backward(H, W, t, ignore_index, **kw)
+    torch.cuda.synchronize()
+    assert lce.device_status() == 0
+    ref = oracle.forward_backward(x_H, x_W, targets, ignore_index)
+    assert abs(loss.item() - ref["loss"]) <= TOL_LOSS, (loss.item(), ref["loss"])
+    assert rel_fro(np64(dH), ref["dH"]) <= TOL_REL
+    assert rel_fro(np64(dW), ref["dW"]) <= TOL_REL
+    return loss, dH, dW
+
+
+def test_single_class_vocab():
+    x = make_inputs("gpt1b", N=300, d=64, V=1, padding=("random_frac", 0.2), seqs=1)
+    H, W, t = to_device(x)
+    loss, dH, dW = lce.lce_forward_backward(H, W, t, IGNORE_INDEX)
+    torch.cuda.synchronize()
+    assert loss.item() == 0.0
+    assert torch.count_nonzero(dH).item() == 0 and torch.count_nonzero(dW).item() == 0
+
+
+@pytest.mark.parametrize("d", [8, 24, 72])
+def test_small_and_ragged_hidden_sizes(d):
+    x = make_inputs("gpt1b", N=500, d=d, V=1300, padding=("random_frac", 0.2), seqs=1)
+    H, W, t = to_device(x)
+    _oracle_check(H, W, t, x.H_f32(), x.W_f32(), x.targets)
+
+
+def test_single_token():
+    for pad in (("none",), ("all",)):
+        x = make_inputs("gpt1b", N=1, d=64, V=700, padding=pad, seqs=1)
+        H, W, t = to_device(x)
+        loss, dH, dW = lce.lce_forward_backward(H, W, t, IGNORE_INDEX)
+        torch.cuda.synchronize()
+        ref = oracle.forward_backward(x.H_f32(), x.W_f32(), x.targets, IGNORE_INDEX)
+        if pad[0] == "all":
+            assert math.isnan(loss.item()) and torch.count_nonzero(dW).item() == 0
+        else:
+            assert abs(loss.item() - ref["loss"]) <= TOL_LOSS
+            assert rel_fro(np64(dW), ref["dW"]) <= TOL_REL
+
+
+def test_extreme_logits_and_last_vocab_target():
+    """Logit std ~30 (exp far outside fp32 without the running max) and
+    targets on the last vocabulary row (the ragged last tile)."""
+    x = make_inputs("gpt1b", N=400, d=128, V=2049, padding=("random_frac", 0.1), seqs=1, w_scale=30.0)
+    x.targets[::7] = 2048
+    H, W, t = to_device(x)
+    loss, dH, dW = _oracle_check(H, W, t, x.H_f32(), x.W_f32(), x.targets)
+    assert math.isfinite(loss.item())
+
+
+def test_other_ignore_index():
+    x = make_inputs("gpt1b", N=600, d=64, V=900, padding=("none",), seqs=1)
+    x.targets[::3] = 0           # class 0 doubles as the padding marker here
+    H, W, t = to_device(x)
+    _oracle_check(H, W, t, x.H_f32(), x.W_f32(), x.targets, ignore_index=0)
