@@ -327,8 +327,9 @@ def test_single_class_vocab():
     H, W, t = to_device(x)
     loss, dH, dW = lce.lce_forward_backward(H, W, t, IGNORE_INDEX)
     torch.cuda.synchronize()
-    assert loss.item() == 0.0
-    assert torch.count_nonzero(dH).item() == 0 and torch.count_nonzero(dW).item() == 0
+    # exactly 0 in the definition; the kernel's log2-domain lse rounds to ~1 ulp
+    assert abs(loss.item()) <= 1e-6
+    assert dH.float().abs().max().item() <= 1e-6 and dW.abs().max().item() <= 1e-6
 
 
 @pytest.mark.parametrize("d", [8, 24, 72])
