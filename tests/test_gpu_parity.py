@@ -368,3 +368,34 @@ def test_other_ignore_index():
     x.targets[::3] = 0           # class 0 doubles as the padding marker here
     H, W, t = to_device(x)
     _oracle_check(H, W, t, x.H_f32(), x.W_f32(), x.targets, ignore_index=0)
+
+
+def test_cuda_graph_capture_and_replay():
+    """lce_run with a caller workspace enqueues kernels only (no host sync, no
+    allocation), so a training step can capture it in a CUDA graph; replays
+    reproduce the eager results bit for bit."""
+    x = make_inputs("gpt1b", N=1024, d=256, V=5000, padding=("random_frac", 0.2), seqs=1)
+    H, W, t = to_device(x)
+    N, d = H.shape
+    V = W.shape[0]
+    ws = torch.empty(lce.workspace_size(N, d, V), dtype=torch.uint8, device="cuda")
+    loss = torch.empty((), dtype=torch.float32, device="cuda")
+    dH = torch.empty_like(H)
+    dW = torch.empty(W.shape, dtype=torch.float32, device="cuda")
+    lce.lce_run(H, W, t, IGNORE_INDEX, loss=loss, dH=dH, dW=dW, workspace=ws)   # warm-up (device set-up)
+    torch.cuda.synchronize()
+    ref = (loss.clone(), dH.clone(), dW.clone())
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        lce.lce_run(H, W, t, IGNORE_INDEX, loss=loss, dH=dH, dW=dW, workspace=ws)
+    for _ in range(2):
+        loss.zero_()
+        dH.zero_()
+        dW.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(loss, ref[0])
+        assert torch.equal(dH.view(torch.int16), ref[1].view(torch.int16))
+        assert torch.equal(dW, ref[2])
