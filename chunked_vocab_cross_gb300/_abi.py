@@ -42,6 +42,7 @@ SIGNATURES = {
     "lce_profile_begin": (c_int, []),
     "lce_profile_end": (c_int, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(c_int64), c_int]),
     "lce_version": (c_int, []),
+    "lce_selftest_wait_timeout": (c_int, [c_int64, c_void_p, c_void_p]),
 }
 
 

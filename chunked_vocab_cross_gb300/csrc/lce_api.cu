@@ -805,6 +805,17 @@ lce_status_t lce_forward_noalloc(const void *H, const void *W, const int64_t *ta
     return lce_run(&a);
 }
 
+lce_status_t lce_selftest_wait_timeout(int64_t cycles, int32_t *gave_up, lce_stream_t stream) {
+    if (!gave_up) return LCE_ERR_NULL;
+    if (cycles < 1 || cycles > (int64_t(1) << 34)) return LCE_ERR_SHAPE;
+    DevInfo *di = nullptr;
+    lce_status_t s = device_info(&di);
+    if (s != LCE_OK) return s;
+    k_wait_selftest<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(cycles, gave_up);
+    LCE_CHECK_LAUNCH();
+    return LCE_OK;
+}
+
 int lce_version(void) { return 100; }
 
 }  // extern "C"

@@ -243,14 +243,15 @@ __device__ inline TileInfo tile_info(const Sched &s, int u, int n) {
     return t;
 }
 
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                         long long limit = kWaitCycles) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const long long t0 = clock64();
     for (;;) {
         if (mbar_try_wait(a, parity)) return true;
         if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > limit) {
             *abort_flag = 1;
             atomicOr(&g_status, DEV_TIMEOUT);
             return false;

@@ -151,6 +151,21 @@ __global__ void __launch_bounds__(256)
     if (lse_user) lse_user[idx[row]] = lse;
 }
 
+// Self-test of the bounded wait every pipeline barrier uses: one thread waits
+// on a fresh mbarrier that nothing will ever complete, with a limit of
+// `cycles` SM clocks. The wait gives up, raises DEV_TIMEOUT in the status
+// word and the kernel returns; *out records 1 if the wait reported failure.
+__global__ void k_wait_selftest(long long cycles, int *out) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+    const bool done = wait_bar(&bar, 0, &abort_flag, cycles);
+    out[0] = done ? 0 : 1;
+}
+
 // Backward from a stored lse: lse2[r] = lse_in[idx[r]] / ln 2 for the
 // compacted rows (the form the G epilogue uses).
 __global__ void __launch_bounds__(256)

@@ -222,6 +222,16 @@ lce_status_t lce_forward_noalloc(const void *H, const void *W, const int64_t *ta
                                  int64_t ignore_index, int64_t N, int64_t d, int64_t V,
                                  float *loss, lce_stream_t stream);
 
+/*
+ * Failure-path self-test: launches one thread that waits on a pipeline
+ * barrier nothing completes, using the same bounded wait as the GEMM kernels
+ * but with a limit of `cycles` SM clocks (1 .. 2^34). The wait gives up,
+ * sets LCE_DEV_TIMEOUT in the device status word and the kernel returns, so
+ * the context stays usable; *gave_up (device int32) receives 1. Read the
+ * status with lce_get_device_status.
+ */
+lce_status_t lce_selftest_wait_timeout(int64_t cycles, int32_t *gave_up, lce_stream_t stream);
+
 /* ABI version: major*10000 + minor*100 + patch. */
 int lce_version(void);
 

@@ -399,3 +399,22 @@ def test_cuda_graph_capture_and_replay():
         assert torch.equal(loss, ref[0])
         assert torch.equal(dH.view(torch.int16), ref[1].view(torch.int16))
         assert torch.equal(dW, ref[2])
+
+
+def test_bounded_wait_times_out_into_the_status_word():
+    """A pipeline wait that nothing completes gives up after its limit, raises
+    LCE_DEV_TIMEOUT and returns; the context stays usable (a full call after
+    it still matches the oracle)."""
+    import ctypes
+    from chunked_vocab_cross_gb300 import _abi
+    lce.device_status()
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r = _abi.lib().lce_selftest_wait_timeout(2_000_000, ctypes.c_void_p(flag.data_ptr()),
+                                             ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert r == 0
+    bits = lce.device_status()
+    assert flag.item() == 1
+    assert bits & 0x2
+    assert lce.device_status() == 0      # reading clears the word
+    x = make_inputs("gpt1b", N=300, d=128, V=1000, padding=("random_frac", 0.1), seqs=1)
+    _run_and_compare(x)
