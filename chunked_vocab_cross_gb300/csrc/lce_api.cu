@@ -2,9 +2,11 @@
 // tensor-map encoding, and the launch sequence of the fused output-projection
 // + cross-entropy path on the caller's stream.
 //
-// Sequence (all on `stream`, no host synchronisation):
+// Sequence (all on `stream`, no host synchronisation), per token chunk
+// (all N rows unless lce_args_t.token_chunk caps it; k_count_valid first
+// counts the call's valid rows when there are several chunks):
 //   1 k_compact        valid rows -> idx / inv / Nv (device)
-//   2 k_gather         Hc = H[idx], zero-padded to 128-row blocks
+//   2 k_gather         Hc = H[idx], zero-padded to 256-row pair blocks
 //   3 k_gemm<LSE>      logits tiles + online log-sum-exp partials + target logit
 //   4 k_lse_merge      lse per row, loss_i
 //   5 k_loss_partial   sum of loss_i (k_loss_final: loss = sum / Nv)
@@ -14,6 +16,7 @@
 //                      dHacc (+)= G_j W[chunk j] (three G buffers; consecutive
 //                      launches overlap through programmatic dependent launch)
 //   7 k_dh_scatter     dH = dHacc[inv], zero on ignored rows
+// and finally k_loss_final (loss = sum of the chunks' sums / Nv).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>

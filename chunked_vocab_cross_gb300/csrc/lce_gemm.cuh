@@ -15,8 +15,8 @@
 //               MMA thread already fills the other accumulator.
 //
 // Tile types (D = A . B^T in TMEM):
-//   T_LSE  S = Hc . W^T       per 128-row block over a contiguous range of
-//          256-wide vocab tiles; the epilogue carries the online (max, sum)
+//   T_LSE  S = Hc . W^T       per 256-row pair block over a contiguous range
+//          of 256-wide vocab tiles; the epilogue carries the online (max, sum)
 //          of exp over the row in registers and writes one (m, l) partial per
 //          row and range, plus the target logit (forward).
 //   T_G    S = Hc . W_c^T     over one vocab chunk (logits recomputed in
@@ -144,7 +144,7 @@ struct GemmArgs {
     const int *tc;         // compacted targets, -1 where none
     // KIND_LSE
     float *z;              // per compacted row: target logit
-    float2 *part;          // (m, l) partials [splits][m_blocks*128]
+    float2 *part;          // (m, l) partials [splits][m_blocks*256]
     // KIND_BWD: dW / dH tiles of the current chunk [v0, v0+vlen) (if has_cur),
     // G tiles of the next chunk [v0n, v0n+vlenn) (if has_next)
     int v0, vlen, v0n, vlenn, has_cur, has_next;
@@ -166,7 +166,7 @@ struct Sched {
     int units;
     // KIND_LSE
     int m_blocks, n_tiles, splits, kseg;
-    // KIND_BWD: task counts and shapes per type (tasks listed dW, dH, G)
+    // KIND_BWD: task counts and shapes per type (tasks listed G, dW, dH)
     int n_dw, n_dh, n_g, nt_d, nt_g, kseg_dw, kseg_dh, kseg_g;
 };
 
