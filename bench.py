@@ -31,8 +31,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per backward k_gemm launch of the llama8b shape,
 # from profiles/k_gemm_pair_llama8b_v16k_ncu_full.md; valid only for the
 # kernel sources it was captured from (sha256 prefix below), else reported null.
-NCU_TRAFFIC = {"workload": "llama8b", "kernel": "backward", "bytes_per_launch": 846.0e6,
-               "src_sha256": "5951da1fc5c00685"}
+NCU_TRAFFIC = {"workload": "llama8b", "kernel": "backward", "bytes_per_launch": 840.9e6,
+               "src_sha256": "f6ad831fa3391a84"}
 
 
 def kernel_src_sha256() -> str:
