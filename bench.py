@@ -29,10 +29,11 @@ METRIC = "fused linear-CE fwd+bwd valid tokens/sec; % of dense BF16 tensor peak"
 UNIT = "valid tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # DRAM bytes (read + write) per backward k_gemm launch of the llama8b shape,
-# from profiles/k_gemm_pair_llama8b_v16k_ncu_full.md; valid only for the
-# kernel sources it was captured from (sha256 prefix below), else reported null.
-NCU_TRAFFIC = {"workload": "llama8b", "kernel": "backward", "bytes_per_launch": 840.9e6,
-               "src_sha256": "f6ad831fa3391a84"}
+# from profiles/k_gemm_pair_llama8b_v24k_ncu_full.md; valid only for the
+# kernel sources it was captured from (sha256 prefix below) and the default
+# vocab chunk, else reported null.
+NCU_TRAFFIC = {"workload": "llama8b", "kernel": "backward", "bytes_per_launch": 1235.0e6,
+               "src_sha256": "13b40ec0684e0a64"}
 
 
 def kernel_src_sha256() -> str:
@@ -357,7 +358,7 @@ def main():
         "device_status": status,
         "clocks": clocks,
         "workspace_bytes": int(ws.numel()),
-        "vocab_chunk": args.vocab_chunk or 4096,
+        "vocab_chunk": args.vocab_chunk or "library default (6144)",
         "logits_bytes_avoided": int(w.N * w.V * 4),
     }
     print(json.dumps(line), flush=True)
