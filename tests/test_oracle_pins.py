@@ -273,3 +273,71 @@ def test_sampled_reference_matches_full():
     assert s["loss"] == pytest.approx(full["loss"], rel=1e-13)
     np.testing.assert_allclose(s["dH_rows"], full["dH"][rows], atol=1e-15)
     np.testing.assert_allclose(s["dW_rows"], full["dW"][vocab], atol=1e-15)
+
+
+# ------------------------------------------------ fused optimizer step (oracle)
+
+def _torch_steps(kind, w0, grads, **hp):
+    torch = pytest.importorskip("torch")
+    p = torch.nn.Parameter(torch.tensor(w0, dtype=torch.float64))
+    if kind == "sgd":
+        opt = torch.optim.SGD([p], lr=hp["lr"], momentum=hp.get("momentum", 0.0),
+                              weight_decay=hp.get("weight_decay", 0.0))
+    else:
+        opt = torch.optim.AdamW([p], lr=hp["lr"], betas=(hp["beta1"], hp["beta2"]), eps=hp["eps"],
+                                weight_decay=hp.get("weight_decay", 0.0))
+    for g in grads:
+        p.grad = torch.tensor(g, dtype=torch.float64)
+        opt.step()
+    st = opt.state[p]
+    m = st.get("momentum_buffer", st.get("exp_avg"))
+    v = st.get("exp_avg_sq")
+    return (p.detach().numpy(), None if m is None else m.numpy(), None if v is None else v.numpy())
+
+
+def _oracle_steps(kind, w0, grads, **hp):
+    w, m, v = np.array(w0), None, None
+    for t, g in enumerate(grads, start=1):
+        r = oracle.optimizer_step(kind, w, g, step=t, exp_avg=m, exp_avg_sq=v, **hp)
+        w, m, v = r["w"], r["exp_avg"], r["exp_avg_sq"]
+    return w, m, v
+
+
+@pytest.mark.parametrize("kind,hp", [
+    ("sgd", dict(lr=0.1)),
+    ("sgd", dict(lr=0.05, momentum=0.9, weight_decay=0.01)),
+    ("adamw", dict(lr=3e-4, beta1=0.9, beta2=0.999, eps=1e-8)),
+    ("adamw", dict(lr=1e-2, beta1=0.8, beta2=0.95, eps=1e-6, weight_decay=0.1)),
+])
+def test_optimizer_step_matches_torch_optim(kind, hp):
+    g = np.random.default_rng(7)
+    w0 = g.standard_normal((6, 5))
+    grads = [g.standard_normal((6, 5)) * s for s in (1.0, 0.3, 2.0, 0.01)]
+    ow, om, ov = _oracle_steps(kind, w0, grads, **hp)
+    tw, tm, tv = _torch_steps(kind, w0, grads, **hp)
+    np.testing.assert_allclose(ow, tw, rtol=1e-13, atol=1e-15)
+    if tm is not None:
+        np.testing.assert_allclose(om, tm, rtol=1e-13, atol=1e-15)
+    if tv is not None:
+        np.testing.assert_allclose(ov, tv, rtol=1e-13, atol=1e-18)
+
+
+def test_adamw_first_step_closed_form():
+    # t = 1: m_hat = g, v_hat = g^2, so w moves by lr * g / (|g| + eps)
+    g = np.array([[3.0, -0.5, 1e-9, 0.0]])
+    w = np.array([[1.0, 2.0, -3.0, 4.0]])
+    r = oracle.optimizer_step("adamw", w, g, lr=0.01, step=1, beta1=0.9, beta2=0.99, eps=1e-8)
+    np.testing.assert_allclose(r["w"], w - 0.01 * g / (np.abs(g) + 1e-8), rtol=1e-14, atol=0)
+
+
+def test_zero_gradient_without_decay_only_decays_the_moments():
+    g0 = np.zeros((3, 4))
+    w = np.arange(12.0).reshape(3, 4)
+    m = np.full((3, 4), 2.0)
+    v = np.full((3, 4), 4.0)
+    r = oracle.optimizer_step("adamw", w, g0, lr=0.1, step=5, beta1=0.9, beta2=0.99, eps=1e-8,
+                              exp_avg=m, exp_avg_sq=v)
+    np.testing.assert_allclose(r["exp_avg"], 0.9 * m)
+    np.testing.assert_allclose(r["exp_avg_sq"], 0.99 * v)
+    s = oracle.optimizer_step("sgd", w, g0, lr=0.1, step=3)
+    np.testing.assert_array_equal(s["w"], w)
