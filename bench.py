@@ -209,6 +209,8 @@ def main():
     ap.add_argument("--vocab", type=int, default=0,
                     help="override V (a smaller case with the same per-launch shape, for profiling)")
     ap.add_argument("--vocab-chunk", type=int, default=0, help="backward vocab chunk (0 = library default)")
+    ap.add_argument("--optim", default="none", choices=["none", "sgd", "adamw"],
+                    help="fuse an optimizer step on W into the backward (no dW buffer; W is updated every step)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
@@ -241,11 +243,22 @@ def main():
     t = t_host.to(dev)
     loss = torch.empty((), dtype=torch.float32, device=dev)
     dH = torch.empty_like(H)
-    dW = torch.empty(W.shape, dtype=torch.float32, device=dev)
-    ws = torch.empty(lce.workspace_size(w.N, w.d, w.V, vocab_chunk=args.vocab_chunk), dtype=torch.uint8, device=dev)
+    fused = args.optim != "none"
+    dW = None if fused else torch.empty(W.shape, dtype=torch.float32, device=dev)
+    ws = torch.empty(lce.workspace_size(w.N, w.d, w.V, vocab_chunk=args.vocab_chunk, fused_optimizer=fused),
+                     dtype=torch.uint8, device=dev)
+    opt = lce.FusedOptimizer(W, args.optim, lr=1e-5) if fused else None
+
+    def run(Hx, tx, lx, dHx):
+        if opt is None:
+            lce.lce_run(Hx, W, tx, -100, loss=lx, dH=dHx, dW=dW, workspace=ws, vocab_chunk=args.vocab_chunk)
+        else:
+            opt.step_count += 1
+            lce.lce_run(Hx, W, tx, -100, loss=lx, dH=dHx, workspace=ws, vocab_chunk=args.vocab_chunk,
+                        optim=opt._optim())
 
     def step():
-        lce.lce_run(H, W, t, -100, loss=loss, dH=dH, dW=dW, workspace=ws, vocab_chunk=args.vocab_chunk)
+        run(H, t, loss, dH)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -287,7 +300,11 @@ def main():
     def e2e_step():
         H_e.copy_(H_host, non_blocking=True)
         t_e.copy_(t_host, non_blocking=True)
-        l, _, _ = lce.lce_forward_backward(H_e, W, t_e, -100, vocab_chunk=args.vocab_chunk)
+        if opt is None:
+            l, _, _ = lce.lce_forward_backward(H_e, W, t_e, -100, vocab_chunk=args.vocab_chunk)
+        else:
+            l = torch.empty((), dtype=torch.float32, device=dev)
+            run(H_e, t_e, l, torch.empty_like(H_e))
         e2e_loss.copy_(l, non_blocking=True)
 
     for _ in range(2):
@@ -323,7 +340,7 @@ def main():
     achieved = flops_launch / (per_launch_ms / 1e3) / 1e12
     traffic = None
     if (NCU_TRAFFIC["workload"] == w.name and NCU_TRAFFIC["kernel"] == name and w.V == 128256
-            and NCU_TRAFFIC["src_sha256"] == kernel_src_sha256() and not args.vocab_chunk):
+            and NCU_TRAFFIC["src_sha256"] == kernel_src_sha256() and not args.vocab_chunk and opt is None):
         traffic = NCU_TRAFFIC["bytes_per_launch"]
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     total_prof = sum(p["ms"] for p in phases.values())
@@ -359,6 +376,7 @@ def main():
         "clocks": clocks,
         "workspace_bytes": int(ws.numel()),
         "vocab_chunk": args.vocab_chunk or "library default (6144)",
+        "fused_optimizer": None if opt is None else f"{args.optim} on W in place (state fp32 [V,d]; no dW buffer)",
         "logits_bytes_avoided": int(w.N * w.V * 4),
     }
     print(json.dumps(line), flush=True)

@@ -19,8 +19,9 @@ PHASE_NAMES = ("compact_gather", "logits_lse", "lse_merge_loss", "backward", "dH
 STATUS = {
     0: "LCE_OK", 1: "LCE_ERR_NULL", 2: "LCE_ERR_SHAPE", 3: "LCE_ERR_ALIGN", 4: "LCE_ERR_DTYPE",
     5: "LCE_ERR_CUDA", 6: "LCE_ERR_WORKSPACE", 7: "LCE_ERR_TARGET_RANGE", 8: "LCE_ERR_TIMEOUT",
-    9: "LCE_ERR_DEVICE",
+    9: "LCE_ERR_DEVICE", 10: "LCE_ERR_ARG",
 }
+LCE_OPT_NONE, LCE_OPT_SGD, LCE_OPT_ADAMW = 0, 1, 2
 
 # Every function include/lce.h declares: name -> (restype, argtypes)
 SIGNATURES = {
@@ -46,6 +47,17 @@ SIGNATURES = {
 }
 
 
+class LceOptim(ctypes.Structure):
+    """Mirror of lce_optim_t."""
+    _fields_ = [
+        ("kind", c_int),
+        ("lr", c_float), ("weight_decay", c_float), ("momentum", c_float),
+        ("beta1", c_float), ("beta2", c_float), ("eps", c_float),
+        ("step", c_int64),
+        ("master_W", c_void_p), ("exp_avg", c_void_p), ("exp_avg_sq", c_void_p),
+    ]
+
+
 class LceArgs(ctypes.Structure):
     """Mirror of lce_args_t."""
     _fields_ = [
@@ -61,6 +73,7 @@ class LceArgs(ctypes.Structure):
         ("lse_in", c_void_p),
         ("grad_loss", c_void_p),
         ("token_chunk", c_int64),
+        ("optim", c_void_p),
     ]
 
 

@@ -41,7 +41,15 @@ constexpr int kMaxSms = 256;              // bound used to size the (m, l) parti
 // G and W rows stay largely L2-resident (6144 measured best of 2048..12288 on
 // all four bf16 workloads).
 constexpr int64_t kDefaultVocabChunk = 6144;
+// G chunk buffers: three for a plain backward (chunk j is read while chunk
+// j+1 is written, and the launch after may already write chunk j+2 while
+// chunk j's last tiles run); four with a fused optimizer, whose dW tiles of
+// chunk j run one launch later (see run_rows).
 constexpr int kGBuffers = 3;
+constexpr int kGBuffersOpt = 4;
+constexpr int kMaxGBuffers = 4;
+
+inline bool has_optim(const lce_args_t *a) { return a->optim && a->optim->kind != LCE_OPT_NONE; }
 
 thread_local int t_last_cuda = 0;
 std::atomic<int64_t> g_launches{0};
@@ -122,7 +130,8 @@ lce_status_t device_info(DevInfo **out) {
         di.major = p.major;
         di.minor = p.minor;
         if (!(di.major == 10 && di.minor == 3) || di.sms > kMaxSms) return LCE_ERR_DEVICE;
-        const void *gemms[] = {(const void *)k_gemm<KIND_LSE>, (const void *)k_gemm<KIND_BWD>};
+        const void *gemms[] = {(const void *)k_gemm<KIND_LSE>, (const void *)k_gemm<KIND_BWD>,
+                               (const void *)k_gemm<KIND_BWD_OPT>};
         for (const void *f : gemms) {
             e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
             if (e != cudaSuccess) {
@@ -206,7 +215,8 @@ struct Layout {
 // Every operand the tensor cores read is bf16. fp32 inputs are carried as bf16
 // hi/lo pairs (Hc/Hc_lo, W_hi/W_lo, G/G_lo), so the fp32 path also holds a
 // split copy of W (4*V*d bytes).
-Layout make_layout(int64_t N, int64_t d, int64_t V, lce_dtype_t dt, int64_t Vc, bool backward, int n_tc = 1) {
+Layout make_layout(int64_t N, int64_t d, int64_t V, lce_dtype_t dt, int64_t Vc, bool backward, int n_tc = 1,
+                   int n_gbuf = kGBuffers) {
     Layout L;
     const bool split = dt == LCE_FP32;
     L.N_pad = (N + kPairM - 1) / kPairM * kPairM;
@@ -233,10 +243,8 @@ Layout make_layout(int64_t N, int64_t d, int64_t V, lce_dtype_t dt, int64_t Vc, 
         L.W_lo = take(static_cast<size_t>(V) * d * 2);
     }
     if (backward) {
-        // three G buffers: chunk j is read while chunk j+1 is written, and the
-        // launch after may already write chunk j+2 while chunk j's last tiles run
-        L.G = take(kGBuffers * L.N_pad * Vc * 2);
-        if (split) L.G_lo = take(kGBuffers * L.N_pad * Vc * 2);
+        L.G = take(n_gbuf * L.N_pad * Vc * 2);
+        if (split) L.G_lo = take(n_gbuf * L.N_pad * Vc * 2);
         L.dHacc = take(L.N_pad * d * 4);
     }
     L.gcount = take(64);               // valid count of the whole call (token chunks)
@@ -258,7 +266,8 @@ lce_status_t check_args(const lce_args_t *a) {
     if (!a) return LCE_ERR_NULL;
     if (a->dtype != LCE_BF16 && a->dtype != LCE_FP32) return LCE_ERR_DTYPE;
     if (!a->H || !a->W || !a->targets) return LCE_ERR_NULL;
-    if ((a->dH == nullptr) != (a->dW == nullptr)) return LCE_ERR_NULL;
+    // dH and dW together, or neither; with a fused optimizer dH alone
+    if (has_optim(a) ? !a->dH : (a->dH == nullptr) != (a->dW == nullptr)) return LCE_ERR_NULL;
     if (a->lse_in ? !a->dH : !a->loss) return LCE_ERR_NULL;   // backward-only needs grads; forward needs loss
     if (a->N < 1 || a->N >= (int64_t(1) << 31) || a->d < 1 || a->d > 65536 || a->V < 1 ||
         a->V >= (int64_t(1) << 31))
@@ -271,6 +280,29 @@ lce_status_t check_args(const lce_args_t *a) {
     if (mis(a->H) || mis(a->W) || (a->dH && mis(a->dH)) || (a->dW && mis(a->dW)) ||
         (a->workspace && mis(a->workspace)))
         return LCE_ERR_ALIGN;
+    if (a->optim) {
+        const lce_optim_t *o = a->optim;
+        if (o->kind != LCE_OPT_NONE && o->kind != LCE_OPT_SGD && o->kind != LCE_OPT_ADAMW) return LCE_ERR_ARG;
+        if (o->kind != LCE_OPT_NONE) {
+            // the update consumes the gradient of the whole call: no dW output,
+            // no accumulation into one, no token chunks
+            if (!a->dH) return LCE_ERR_NULL;
+            if (a->dW || a->accumulate_dW || token_rows(a->N, a->token_chunk) != a->N) return LCE_ERR_ARG;
+            if (o->master_W && a->dtype != LCE_BF16) return LCE_ERR_ARG;
+            if (!(o->lr >= 0.f) || !(o->weight_decay >= 0.f) || o->step < 1) return LCE_ERR_ARG;
+            if (o->kind == LCE_OPT_ADAMW) {
+                if (!o->exp_avg || !o->exp_avg_sq) return LCE_ERR_NULL;
+                if (!(o->beta1 >= 0.f && o->beta1 < 1.f && o->beta2 >= 0.f && o->beta2 < 1.f && o->eps > 0.f))
+                    return LCE_ERR_ARG;
+            } else {
+                if (!(o->momentum >= 0.f)) return LCE_ERR_ARG;
+                if (o->momentum != 0.f && !o->exp_avg) return LCE_ERR_NULL;
+            }
+            if ((o->master_W && mis(o->master_W)) || (o->exp_avg && mis(o->exp_avg)) ||
+                (o->exp_avg_sq && mis(o->exp_avg_sq)))
+                return LCE_ERR_ALIGN;
+        }
+    }
     return LCE_OK;
 }
 
@@ -389,24 +421,32 @@ lce_status_t run_rows(const lce_args_t *a, const DevInfo &di, uint8_t *base, con
     }
     if (!backward) return LCE_OK;
 
-    // Backward: launch j runs the G tiles of chunk j+1 (writing G buffer
-    // (j+1)%3) and dW/dH of chunk j (reading buffer j%3); launch j = -1 only
-    // fills G of chunk 0 and the last launch has no next chunk. Launches after
-    // the first are programmatic dependents of their predecessor: their CTAs
-    // start as the predecessor's finish, and wait for it (griddepcontrol.wait)
-    // before their dW/dH tiles. A launch signals its own dependent only after
-    // that wait, so launch j+1 (writing buffer (j+2)%3 = (j-1)%3) cannot start
-    // before launch j-1, the last reader of that buffer, has completed.
+    // Backward. Plain: launch j runs the G tiles of chunk j+1 (writing G
+    // buffer (j+1)%3) and dW/dH of chunk j (reading buffer j%3); launch j = -1
+    // only fills G of chunk 0 and the last launch has no next chunk. Launches
+    // after the first are programmatic dependents of their predecessor: their
+    // CTAs start as the predecessor's finish, and wait for it
+    // (griddepcontrol.wait) before their dW/dH tiles. A launch signals its own
+    // dependent only after that wait, so launch j+1 (writing buffer
+    // (j+2)%3 = (j-1)%3) cannot start before launch j-1, the last reader of
+    // that buffer, has completed.
+    // With a fused optimizer the dW tiles of chunk j (which rewrite W rows of
+    // chunk j) move to launch j+1, after its wait: launch j, whose dH tiles
+    // are the last readers of those rows, has completed by then. Launch j
+    // then reads buffers j%4 (dH) and (j-1)%4 (dW) while writing (j+1)%4, and
+    // its dependent writes (j+2)%4 = (j-2)%4, last read in launch j-1.
+    const bool opt = has_optim(a);
+    const int nbuf = opt ? kGBuffersOpt : kGBuffers;
     const size_t gbuf = static_cast<size_t>(L.N_pad) * Vc;   // elements per G buffer
     const bool mn3d_d = (d % kAtom) == 0;
-    GemmMaps maps_bwd[kGBuffers];
-    memset(maps_bwd, 0, sizeof(maps_bwd));
-    for (int b = 0; b < kGBuffers; ++b) {
+    OperandMaps dh_maps[kMaxGBuffers], dw_maps[kMaxGBuffers];
+    memset(dh_maps, 0, sizeof(dh_maps));
+    memset(dw_maps, 0, sizeof(dw_maps));
+    for (int b = 0; b < nbuf; ++b) {
         const __nv_bfloat16 *Gb = G + b * gbuf;
         const __nv_bfloat16 *Gb_lo = G_lo + b * gbuf;
-        maps_bwd[b].t[map_slot(T_G)] = maps_lse.t[map_slot(T_LSE)];
-        OperandMaps &dh = maps_bwd[b].t[map_slot(T_DH)];
-        OperandMaps &dw = maps_bwd[b].t[map_slot(T_DW)];
+        OperandMaps &dh = dh_maps[b];
+        OperandMaps &dw = dw_maps[b];
         if (!encode_map(&dh.A[0], Gb, Vc, L.N_pad, kBK, kBM) || !encode_map(&dh.A[1], Gb_lo, Vc, L.N_pad, kBK, kBM) ||
             !encode_map_mn3(&dw.A[0], Gb, Vc, L.N_pad, kBK, kBM / kAtom) ||
             !encode_map_mn3(&dw.A[1], Gb_lo, Vc, L.N_pad, kBK, kBM / kAtom))
@@ -423,48 +463,83 @@ lce_status_t run_rows(const lce_args_t *a, const DevInfo &di, uint8_t *base, con
             return LCE_ERR_CUDA;
         }
     }
-    CUtensorMap st_g[kGBuffers][2], st_dw, st_dh;
-    for (int b = 0; b < kGBuffers; ++b)
+    CUtensorMap st_g[kMaxGBuffers][2], st_dw, st_dh;
+    memset(&st_dw, 0, sizeof(st_dw));
+    for (int b = 0; b < nbuf; ++b)
         if (!encode_store_map(&st_g[b][0], G + b * gbuf, false, Vc, L.N_pad) ||
             !encode_store_map(&st_g[b][1], G_lo + b * gbuf, false, Vc, L.N_pad))
             return LCE_ERR_CUDA;
-    if (!encode_store_map(&st_dw, a->dW, true, d, V) || !encode_store_map(&st_dh, dHacc, true, d, L.N_pad))
+    if ((a->dW && !encode_store_map(&st_dw, a->dW, true, d, V)) || !encode_store_map(&st_dh, dHacc, true, d, L.N_pad))
         return LCE_ERR_CUDA;
-    for (int b = 0; b < kGBuffers; ++b) {
-        maps_bwd[b].st_dw = st_dw;
-        maps_bwd[b].st_dh = st_dh;
+
+    OptArgs oa{};
+    if (opt) {
+        const lce_optim_t *o = a->optim;
+        oa.kind = o->kind == LCE_OPT_ADAMW ? OPT_ADAMW : OPT_SGD;
+        oa.first = o->step == 1;
+        oa.lr = o->lr;
+        oa.wd = o->weight_decay;
+        oa.momentum = o->momentum;
+        oa.beta1 = o->beta1;
+        oa.beta2 = o->beta2;
+        oa.eps = o->eps;
+        if (oa.kind == OPT_ADAMW) {
+            const double t = static_cast<double>(o->step);
+            oa.step_size = static_cast<float>(o->lr / (1.0 - pow(static_cast<double>(o->beta1), t)));
+            oa.inv_bc2_sqrt = static_cast<float>(1.0 / sqrt(1.0 - pow(static_cast<double>(o->beta2), t)));
+        }
+        oa.W = const_cast<void *>(a->W);
+        oa.w_fp32 = a->dtype == LCE_FP32;
+        oa.master = o->master_W;
+        oa.m = o->exp_avg;
+        oa.v = o->exp_avg_sq;
     }
+
     const int n_chunks = static_cast<int>((a->V + Vc - 1) / Vc);
+    auto chunk_len = [&](int c) { return static_cast<int>(a->V - c * Vc < Vc ? a->V - c * Vc : Vc); };
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    void (*bwd_kernel)(const GemmMaps, const GemmArgs) = opt ? k_gemm<KIND_BWD_OPT> : k_gemm<KIND_BWD>;
     {
         PhaseScope ph(3, st);
-        for (int j = -1; j < n_chunks; ++j) {
+        const int last = opt ? n_chunks : n_chunks - 1;
+        for (int j = -1; j <= last; ++j) {
+            const int cw = opt ? j - 1 : j;   // chunk whose dW tiles this launch runs
             GemmArgs g = ga;
             g.lse2 = lse2;
-            g.has_cur = j >= 0;
+            g.has_cur = j >= 0 && j < n_chunks;
             g.has_next = j + 1 < n_chunks;
+            g.has_dw = cw >= 0 && cw < n_chunks;
             if (g.has_cur) {
                 g.v0 = static_cast<int>(j * Vc);
-                g.vlen = static_cast<int>(a->V - g.v0 < Vc ? a->V - g.v0 : Vc);
+                g.vlen = chunk_len(j);
             }
             if (g.has_next) {
                 g.v0n = static_cast<int>((j + 1) * Vc);
-                g.vlenn = static_cast<int>(a->V - g.v0n < Vc ? a->V - g.v0n : Vc);
+                g.vlenn = chunk_len(j + 1);
+            }
+            if (g.has_dw) {
+                g.v0w = static_cast<int>(cw * Vc);
+                g.vlenw = chunk_len(cw);
             }
             g.mn3d = 1 | (mn3d_d ? 6 : 0);
             g.dW = a->dW;
             g.acc_dw = ctx.acc_dw ? 1 : 0;
             g.dH_acc = dHacc;
             g.acc_dh = j > 0 ? 1 : 0;
-            GemmMaps mp = maps_bwd[j < 0 ? 0 : j % kGBuffers];
-            if (g.has_next) {
-                mp.st_g[0] = st_g[(j + 1) % kGBuffers][0];
-                mp.st_g[1] = st_g[(j + 1) % kGBuffers][1];
-            }
+            g.opt = oa;
+            // every slot holds a valid map (buffer 0 where a tile type is absent)
+            GemmMaps mp;
+            mp.t[map_slot(T_G)] = maps_lse.t[map_slot(T_LSE)];
+            mp.t[map_slot(T_DH)] = dh_maps[g.has_cur ? j % nbuf : 0];
+            mp.t[map_slot(T_DW)] = dw_maps[g.has_dw ? cw % nbuf : 0];
+            mp.st_g[0] = st_g[g.has_next ? (j + 1) % nbuf : 0][0];
+            mp.st_g[1] = st_g[g.has_next ? (j + 1) % nbuf : 0][1];
+            mp.st_dw = st_dw;
+            mp.st_dh = st_dh;
             if (j < 0) {
-                k_gemm<KIND_BWD><<<grid, kThreads, kGemmSmem, st>>>(mp, g);
+                bwd_kernel<<<grid, kThreads, kGemmSmem, st>>>(mp, g);
             } else {
                 cudaLaunchConfig_t cfg = {};
                 cfg.gridDim = dim3(grid);
@@ -473,7 +548,7 @@ lce_status_t run_rows(const lce_args_t *a, const DevInfo &di, uint8_t *base, con
                 cfg.stream = st;
                 cfg.attrs = pdl;
                 cfg.numAttrs = 1;
-                cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm<KIND_BWD>, mp, g);
+                cudaError_t e = cudaLaunchKernelEx(&cfg, bwd_kernel, mp, g);
                 if (e != cudaSuccess) {
                     t_last_cuda = e;
                     return LCE_ERR_CUDA;
@@ -498,7 +573,8 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
     const int64_t Vc = pick_chunk(a->V, a->vocab_chunk);
     const int64_t C = token_rows(a->N, a->token_chunk);
     const int n_tc = static_cast<int>((a->N + C - 1) / C);
-    const Layout L = make_layout(C, a->d, a->V, a->dtype, Vc, backward, n_tc);
+    const Layout L = make_layout(C, a->d, a->V, a->dtype, Vc, backward, n_tc,
+                                 has_optim(a) ? kGBuffersOpt : kGBuffers);
 
     WsGuard ws;
     ws.s = st;
@@ -691,7 +767,9 @@ size_t lce_workspace_size_args(const lce_args_t *a) {
     if (a->vocab_chunk < 0 || (a->vocab_chunk > 0 && a->vocab_chunk % kBN) || a->token_chunk < 0) return 0;
     const int64_t C = token_rows(a->N, a->token_chunk);
     const int n_tc = static_cast<int>((a->N + C - 1) / C);
-    return make_layout(C, a->d, a->V, a->dtype, pick_chunk(a->V, a->vocab_chunk), a->dH != nullptr, n_tc).total;
+    return make_layout(C, a->d, a->V, a->dtype, pick_chunk(a->V, a->vocab_chunk), a->dH != nullptr, n_tc,
+                       has_optim(a) ? kGBuffersOpt : kGBuffers)
+        .total;
 }
 
 lce_status_t lce_get_device_status(lce_stream_t stream, int32_t *bits) {
@@ -731,6 +809,7 @@ const char *lce_status_string(lce_status_t s) {
         case LCE_ERR_TARGET_RANGE: return "a non-ignored target is outside [0, V)";
         case LCE_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up";
         case LCE_ERR_DEVICE: return "the current device is not sm_103";
+        case LCE_ERR_ARG: return "unsupported combination of options";
     }
     return "unknown status";
 }
@@ -823,6 +902,6 @@ lce_status_t lce_selftest_wait_timeout(int64_t cycles, int32_t *gave_up, lce_str
     return LCE_OK;
 }
 
-int lce_version(void) { return 100; }
+int lce_version(void) { return 200; }
 
 }  // extern "C"

@@ -23,7 +23,9 @@
 //          backward); the epilogue forms G = (exp(S - lse) - onehot) * scale/Nv
 //          and stores it (bf16).
 //   T_DW   dW_c = G^T . Hc    (M = chunk vocab rows, K = valid tokens); A and
-//          B are read MN-major straight from G and Hc.
+//          B are read MN-major straight from G and Hc. With a fused optimizer
+//          the epilogue applies the SGD / AdamW update to those W rows
+//          instead of storing dW (no dW buffer exists).
 //   T_DH   dHacc (+)= G . W_c (M = valid tokens, K = chunk vocab rows); B is
 //          read MN-major straight from W.
 //
@@ -114,7 +116,10 @@ __host__ __device__ inline long long lse_partial_rows(int rows_cap, int pairs) {
 // launches overlap (programmatic dependent launch): a launch's G tiles start
 // on the SMs its predecessor frees, and its dW/dH tiles wait for the
 // predecessor (which wrote G_j and the dH accumulator) to complete.
-enum Kind : int { KIND_LSE = 0, KIND_BWD = 1 };
+// KIND_BWD_OPT is KIND_BWD with an optimizer step fused into the dW
+// epilogue: its own instantiation, so the plain backward keeps its register
+// allocation.
+enum Kind : int { KIND_LSE = 0, KIND_BWD = 1, KIND_BWD_OPT = 2 };
 enum TileType : int { T_LSE = 0, T_G = 1, T_DH = 2, T_DW = 3 };
 
 // Operand tensor maps per tile type: slot 0 = LSE / G (A = Hc K-major,
@@ -135,6 +140,24 @@ struct GemmMaps {
 
 __host__ __device__ constexpr int map_slot(int type) { return type == T_DH ? 1 : (type == T_DW ? 2 : 0); }
 
+enum OptKind : int { OPT_NONE = 0, OPT_SGD = 1, OPT_ADAMW = 2 };
+
+// Optimizer update fused into the dW epilogue (the gradient of W never
+// reaches memory). SGD: g' = g + wd*w; with momentum b = g' on the first step,
+// else b = momentum*b + g', and g' = b; w -= lr*g'. AdamW (decoupled decay):
+// w *= 1 - lr*wd; m = b1*m + (1-b1)*g; v = b2*v + (1-b2)*g^2;
+// w -= step_size * m / (sqrt(v) * inv_bc2_sqrt + eps), with
+// step_size = lr / (1 - b1^t) and inv_bc2_sqrt = 1 / sqrt(1 - b2^t).
+struct OptArgs {
+    int kind;              // OptKind
+    int first;             // SGD: this step starts the momentum buffer
+    float lr, wd, momentum, beta1, beta2, eps, step_size, inv_bc2_sqrt;
+    void *W;               // [V][d] weights updated in place: bf16, or fp32 when w_fp32
+    int w_fp32;
+    float *master;         // optional fp32 [V][d] master copy of a bf16 W (W = its bf16 rounding)
+    float *m, *v;          // fp32 [V][d]: AdamW moments / SGD momentum buffer (m)
+};
+
 struct GemmArgs {
     const int *counters;   // counters[0] = valid rows this launch tiles (written by the compaction kernel)
     const int *nv_norm;    // *nv_norm = Nv of the whole call, the loss normaliser
@@ -145,9 +168,11 @@ struct GemmArgs {
     // KIND_LSE
     float *z;              // per compacted row: target logit
     float2 *part;          // (m, l) partials [splits][m_blocks*256]
-    // KIND_BWD: dW / dH tiles of the current chunk [v0, v0+vlen) (if has_cur),
-    // G tiles of the next chunk [v0n, v0n+vlenn) (if has_next)
-    int v0, vlen, v0n, vlenn, has_cur, has_next;
+    // KIND_BWD: dH tiles of the current chunk [v0, v0+vlen) (if has_cur),
+    // dW tiles of chunk [v0w, v0w+vlenw) (if has_dw: the current chunk, or
+    // the previous one when an optimizer update is fused), G tiles of the
+    // next chunk [v0n, v0n+vlenn) (if has_next)
+    int v0, vlen, v0n, vlenn, has_cur, has_next, v0w, vlenw, has_dw;
     const float *lse2;     // per compacted row: lse / ln 2
     float *dW;             // [V][d]
     int acc_dw;            // add into dW instead of overwriting
@@ -160,6 +185,7 @@ struct GemmArgs {
     // (one {64, 64} box per column block); 3-D needs the MN extent to be a
     // multiple of 64. Bit 0: DW's A (G), bit 1: DW's B (Hc), bit 2: DH's B (W).
     int mn3d;
+    OptArgs opt;
 };
 
 struct Sched {
@@ -186,7 +212,7 @@ __device__ inline Sched make_sched(const GemmArgs &a, int nv) {
     } else {
         s.nt_d = cdiv(a.d, kBN);
         s.nt_g = a.has_next ? cdiv(a.vlenn, kBN) : 0;
-        s.n_dw = a.has_cur ? cdiv(a.vlen, kPairM) * s.nt_d : 0;
+        s.n_dw = a.has_dw ? cdiv(a.vlenw, kPairM) * s.nt_d : 0;
         s.n_dh = a.has_cur ? cdiv(nv, kPairM) * s.nt_d : 0;
         s.n_g = a.has_next ? cdiv(nv, kPairM) * s.nt_g : 0;
         s.kseg_dw = cdiv(nv, kBK);
@@ -279,6 +305,89 @@ __device__ __forceinline__ void split_bf16(float x, float &hi, float &lo) {
     const float h = __bfloat162float(__float2bfloat16_rn(x));
     lo = x - h;
     hi = h;
+}
+
+// Fused optimizer step on elements [off, off + ncol) of W (ncol a multiple of
+// 8, at most 32, zero for none; off a multiple of 8), split in two so that a
+// chunk's global loads are all in flight together (and with the TMEM load of
+// its gradient): opt_load reads the weights and state, opt_apply updates them
+// with gradient g and writes them back.
+struct OptRegs {
+    float w[32], m[32], v[32];
+};
+
+__device__ __forceinline__ void ld8(const float *p, float *x, bool stream) {
+    const float4 a = stream ? __ldcs(reinterpret_cast<const float4 *>(p)) : *reinterpret_cast<const float4 *>(p);
+    const float4 b = stream ? __ldcs(reinterpret_cast<const float4 *>(p) + 1) : *(reinterpret_cast<const float4 *>(p) + 1);
+    x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+}
+
+__device__ __forceinline__ void st8(float *p, const float *x, bool stream) {
+    const float4 a = make_float4(x[0], x[1], x[2], x[3]), b = make_float4(x[4], x[5], x[6], x[7]);
+    if (stream) {
+        __stcs(reinterpret_cast<float4 *>(p), a);
+        __stcs(reinterpret_cast<float4 *>(p) + 1, b);
+    } else {
+        *reinterpret_cast<float4 *>(p) = a;
+        *(reinterpret_cast<float4 *>(p) + 1) = b;
+    }
+}
+
+__device__ __forceinline__ void opt_load(const OptArgs &o, size_t off, int ncol, OptRegs &s) {
+    const bool use_m = o.kind == OPT_ADAMW || o.momentum != 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (q * 8 < ncol) {
+            const size_t e = off + q * 8;
+            if (o.master || o.w_fp32) {
+                ld8((o.master ? o.master : static_cast<const float *>(o.W)) + e, s.w + q * 8, false);
+            } else {
+                const uint4 x = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(o.W) + e);
+                const uint32_t u[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    s.w[q * 8 + 2 * k] = __uint_as_float(u[k] << 16);
+                    s.w[q * 8 + 2 * k + 1] = __uint_as_float(u[k] & 0xffff0000u);
+                }
+            }
+            if (use_m) ld8(o.m + e, s.m + q * 8, true);
+            if (o.kind == OPT_ADAMW) ld8(o.v + e, s.v + q * 8, true);
+        }
+    }
+}
+
+__device__ __forceinline__ void opt_apply(const OptArgs &o, size_t off, int ncol, OptRegs &s, const float (&g)[32]) {
+    const bool use_m = o.kind == OPT_ADAMW || o.momentum != 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        if (o.kind == OPT_ADAMW) {
+            s.w[j] *= 1.f - o.lr * o.wd;
+            s.m[j] = o.beta1 * s.m[j] + (1.f - o.beta1) * g[j];
+            s.v[j] = o.beta2 * s.v[j] + (1.f - o.beta2) * g[j] * g[j];
+            s.w[j] -= o.step_size * s.m[j] / (sqrtf(s.v[j]) * o.inv_bc2_sqrt + o.eps);
+        } else {
+            float d = g[j] + o.wd * s.w[j];
+            if (use_m) {
+                s.m[j] = o.first ? d : o.momentum * s.m[j] + d;
+                d = s.m[j];
+            }
+            s.w[j] -= o.lr * d;
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (q * 8 < ncol) {
+            const size_t e = off + q * 8;
+            const float *w = s.w + q * 8;
+            if (use_m) st8(o.m + e, s.m + q * 8, true);
+            if (o.kind == OPT_ADAMW) st8(o.v + e, s.v + q * 8, true);
+            if (o.master || o.w_fp32) st8((o.master ? o.master : static_cast<float *>(o.W)) + e, w, false);
+            if (!o.w_fp32)
+                *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(o.W) + e) =
+                    make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]), pack_bf16x2(w[4], w[5]),
+                               pack_bf16x2(w[6], w[7]));
+        }
+    }
 }
 
 // Issue this CTA's TMA loads of one k-block (A rows am.., B rows bn.., k0..)
@@ -394,7 +503,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 unit_range<KIND>(s, u, n0, n1);
                 for (int n = n0; ok && n < n1; ++n) {
                     const TileInfo t = tile_info<KIND>(s, u, n);
-                    if (KIND == KIND_BWD && !dep_done && t.type != T_G) {
+                    if (KIND != KIND_LSE && !dep_done && t.type != T_G) {
                         // dW / dH read what the previous launch wrote
                         griddep_wait();
                         griddep_launch_dependents();
@@ -423,7 +532,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (KIND == KIND_BWD && !dep_done) {
+            if (KIND != KIND_LSE && !dep_done) {
                 // the next launch may only start once the one before this has finished
                 griddep_wait();
                 griddep_launch_dependents();
@@ -500,7 +609,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int grow = 0;
             for (int n = n0; n < n1; ++n, ++tile) {
                 const TileInfo t = tile_info<KIND>(s, u, n);
-                if (KIND == KIND_BWD && !dep_done && t.type != T_G) {
+                if (KIND != KIND_LSE && !dep_done && t.type != T_G) {
                     griddep_wait();   // the dH accumulator / dW rows of the previous launch
                     dep_done = true;
                 }
@@ -522,12 +631,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN;
+                const bool opt_dw = KIND == KIND_BWD_OPT && t.type == T_DW;
 #pragma unroll 1
                 for (int c = 0; c < kBN / 32; ++c) {
+                    const int col = t.nt * kBN + c * 32;   // column within the vocab range / d
+                    // fused optimizer: this thread's W row slice [off, off + ncol)
+                    const size_t opt_off = static_cast<size_t>(a.v0w + grow) * a.d + col;
+                    const int opt_ncol = (opt_dw && grow < a.vlenw && col < a.d) ? (a.d - col < 32 ? a.d - col : 32) : 0;
+                    OptRegs ost;
+                    if (opt_ncol) opt_load(a.opt, opt_off, opt_ncol, ost);
                     uint32_t r[32];
                     tmem_ld32(tbase + c * 32, r);
                     tmem_ld_wait();
-                    const int col = t.nt * kBN + c * 32;   // column within the vocab range / d
                     if (t.type == T_LSE) {
                         const int rel = tgt - col;
                         if (static_cast<unsigned>(rel) < 32u) {
@@ -568,6 +683,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int j = 0; j < 32; ++j) v[j] = zero_acc ? 0.f : __uint_as_float(r[j]);
                         }
+                        if (opt_dw) {
+                            // fused optimizer: update the W row slice in place, no dW store
+                            if (opt_ncol) opt_apply(a.opt, opt_off, opt_ncol, ost, v);
+                            continue;
+                        }
                         uint8_t *sbuf = stage_mine + ebuf * kEpiBufBytes;
                         if (lane == 0) bulk_wait_group_read<1>();   // this buffer's store of two chunks ago has read it
                         __syncwarp();
@@ -607,9 +727,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             } else if (t.type == T_DW) {
                                 // rows past V (last chunk) are clipped by the map
                                 if (a.acc_dw)
-                                    tma_reduce_add_2d(&maps.st_dw, sbuf, col, a.v0 + row0);
+                                    tma_reduce_add_2d(&maps.st_dw, sbuf, col, a.v0w + row0);
                                 else
-                                    tma_store_2d(&maps.st_dw, sbuf, col, a.v0 + row0);
+                                    tma_store_2d(&maps.st_dw, sbuf, col, a.v0w + row0);
                             } else {
                                 if (a.acc_dh)
                                     tma_reduce_add_2d(&maps.st_dh, sbuf, col, row0);

@@ -32,19 +32,24 @@ def _check_inputs(H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor):
 
 
 def workspace_size(N: int, d: int, V: int, dtype=torch.bfloat16, vocab_chunk: int = 0, token_chunk: int = 0,
-                   backward: bool = True) -> int:
+                   backward: bool = True, fused_optimizer: bool = False) -> int:
     a = _abi.LceArgs()
     a.dtype = _DT[dtype]
     a.N, a.d, a.V = N, d, V
     a.vocab_chunk, a.token_chunk = vocab_chunk, token_chunk
     a.dH = 1 if backward else None      # only whether gradients are wanted matters
+    o = _abi.LceOptim()
+    if fused_optimizer:
+        o.kind = _abi.LCE_OPT_SGD
+        a.optim = ctypes.addressof(o)
     return int(_abi.lib().lce_workspace_size_args(ctypes.byref(a)))
 
 
 def lce_run(H, W, targets, ignore_index: int = -100, *, loss=None, dH=None, dW=None, accumulate_dW: bool = False,
             grad_scale: float = 1.0, lse=None, workspace=None, vocab_chunk: int = 0, lse_in=None, grad_loss=None,
-            token_chunk: int = 0, stream=None) -> None:
-    """Raw lce_run over caller-provided output tensors."""
+            token_chunk: int = 0, optim=None, stream=None) -> None:
+    """Raw lce_run over caller-provided output tensors. `optim` is an
+    _abi.LceOptim (a fused optimizer step on W) or None."""
     _check_inputs(H, W, targets)
     a = _abi.LceArgs()
     a.dtype = _DT[H.dtype]
@@ -65,6 +70,7 @@ def lce_run(H, W, targets, ignore_index: int = -100, *, loss=None, dH=None, dW=N
         a.workspace_bytes = workspace.numel() * workspace.element_size()
     a.vocab_chunk = int(vocab_chunk)
     a.token_chunk = int(token_chunk)
+    a.optim = ctypes.addressof(optim) if optim is not None else None
     a.stream = _stream(stream)
     _abi.check(_abi.lib().lce_run(ctypes.byref(a)), "lce_run")
 
@@ -232,3 +238,62 @@ def linear_cross_entropy(H, W, targets, ignore_index: int = -100, fused: bool = 
     if fused:
         return _LinearCrossEntropy.apply(H, W, targets, ignore_index)
     return _LinearCrossEntropySplit.apply(H, W, targets, ignore_index)
+
+
+class FusedOptimizer:
+    """SGD or AdamW on the vocabulary matrix W, applied inside the backward
+    pass of lce_run (the optimizer item of include/lce.h): each call of step()
+    returns the loss and dH for the current W and leaves W updated, without a
+    gradient buffer for W ever existing. Holds the fp32 state (moments,
+    momentum buffer, optional fp32 master weights of a bf16 W) on W's device.
+
+    The pages' training loop attaches an optimizer with algorithm "adamw" or
+    "sgd" that updates weights in place during backward ("OjasX 0.6.1:
+    Training a 1B-Parameter LLM in 6.35GB of RAM", usage listing)."""
+
+    def __init__(self, W: torch.Tensor, algorithm: str = "adamw", lr: float = 3e-4, betas=(0.9, 0.999),
+                 eps: float = 1e-8, weight_decay: float = 0.0, momentum: float = 0.0, master_weights: bool = False):
+        if algorithm not in ("adamw", "sgd"):
+            raise ValueError("algorithm must be 'adamw' or 'sgd'")
+        if not W.is_cuda or not W.is_contiguous() or W.dtype not in _DT:
+            raise ValueError("W must be a contiguous bf16 or fp32 CUDA tensor")
+        if master_weights and W.dtype != torch.bfloat16:
+            raise ValueError("master weights are kept for a bf16 W only")
+        self.W = W
+        self.algorithm = algorithm
+        self.lr, self.betas, self.eps = float(lr), (float(betas[0]), float(betas[1])), float(eps)
+        self.weight_decay, self.momentum = float(weight_decay), float(momentum)
+        self.step_count = 0
+        z = lambda: torch.zeros(W.shape, dtype=torch.float32, device=W.device)  # noqa: E731
+        self.exp_avg = z() if (algorithm == "adamw" or momentum != 0.0) else None
+        self.exp_avg_sq = z() if algorithm == "adamw" else None
+        self.master = W.float() if master_weights else None
+
+    def _optim(self) -> "_abi.LceOptim":
+        o = _abi.LceOptim()
+        o.kind = _abi.LCE_OPT_ADAMW if self.algorithm == "adamw" else _abi.LCE_OPT_SGD
+        o.lr, o.weight_decay, o.momentum = self.lr, self.weight_decay, self.momentum
+        o.beta1, o.beta2 = self.betas
+        o.eps = self.eps
+        o.step = self.step_count
+        o.master_W = self.master.data_ptr() if self.master is not None else None
+        o.exp_avg = self.exp_avg.data_ptr() if self.exp_avg is not None else None
+        o.exp_avg_sq = self.exp_avg_sq.data_ptr() if self.exp_avg_sq is not None else None
+        return o
+
+    def step(self, H, targets, ignore_index: int = -100, *, grad_scale: float = 1.0, grad_loss=None,
+             lse_in=None, vocab_chunk: int = 0, workspace=None, stream=None):
+        """One forward + backward + update of W. Returns (loss, dH); with
+        lse_in (a stored per-row lse of the current W) the forward is skipped
+        and loss is None."""
+        self.step_count += 1
+        loss = None if lse_in is not None else torch.empty((), dtype=torch.float32, device=H.device)
+        dH = torch.empty_like(H)
+        try:
+            lce_run(H, self.W, targets, ignore_index, loss=loss, dH=dH, grad_scale=grad_scale, grad_loss=grad_loss,
+                    lse_in=lse_in, vocab_chunk=vocab_chunk, workspace=workspace, optim=self._optim(),
+                    stream=stream)
+        except Exception:
+            self.step_count -= 1
+            raise
+        return loss, dH

@@ -73,7 +73,8 @@ typedef enum {
     LCE_ERR_WORKSPACE = 6,    /* workspace_bytes below lce_workspace_size() */
     LCE_ERR_TARGET_RANGE = 7, /* device: a non-ignored target outside [0, V) */
     LCE_ERR_TIMEOUT = 8,      /* device: a bounded wait inside a kernel gave up */
-    LCE_ERR_DEVICE = 9        /* current device is not sm_103 */
+    LCE_ERR_DEVICE = 9,       /* current device is not sm_103 */
+    LCE_ERR_ARG = 10          /* an option value or combination that is not supported */
 } lce_status_t;
 
 typedef enum { LCE_BF16 = 0, LCE_FP32 = 1 } lce_dtype_t;
@@ -113,17 +114,56 @@ lce_status_t lce_forward_backward(const void *H, const void *W, const int64_t *t
 lce_status_t lce_compact(const int64_t *targets, int64_t N, int64_t ignore_index, int64_t V,
                          int32_t *idx, int32_t *inv, int32_t *counts, lce_stream_t stream);
 
+/*
+ * Optimizer step on W fused into the backward (lce_args_t.optim): the
+ * gradient of W is consumed where it is produced, in the epilogue of each dW
+ * tile, and never stored — no V x d gradient buffer exists, the "zero-byte
+ * persistent .grad buffers" item of "OjasX 0.6.1: Training a 1B-Parameter LLM
+ * in 6.35GB of RAM" (section "Core Technology"; its usage listing attaches an
+ * "adamw" or "sgd" optimizer that updates weights in place during backward).
+ * The pages do not define the two rules; these follow PyTorch's SGD and AdamW
+ * (no dampening, no Nesterov, no amsgrad), with g the gradient of W
+ * (grad_scale and grad_loss applied):
+ *   SGD:   g += weight_decay * w; with momentum != 0: b = g on step 1, else
+ *          b = momentum * b + g, and g = b (b in exp_avg); w -= lr * g.
+ *   AdamW: w *= 1 - lr * weight_decay; m = beta1*m + (1-beta1)*g;
+ *          v = beta2*v + (1-beta2)*g^2;
+ *          w -= lr/(1-beta1^step) * m / (sqrt(v)/sqrt(1-beta2^step) + eps)
+ *          (m in exp_avg, v in exp_avg_sq).
+ * W is updated in place in its own dtype (bf16 rounded to nearest), or, for
+ * bf16 W with master_W given, the fp32 master copy is updated and W is
+ * rewritten as its bf16 rounding. Every W row is updated exactly once per
+ * call, after the last read of its old value (loss, lse and dH are those of
+ * the old W). State arrays are fp32 [V,d], device, 16-byte aligned, owned by
+ * the caller. Requirements (else LCE_ERR_ARG / LCE_ERR_NULL): dH given and
+ * dW NULL, accumulate_dW 0, one token chunk, step >= 1, lr >= 0,
+ * weight_decay >= 0, 0 <= beta1, beta2 < 1, eps > 0, master_W only for bf16.
+ */
+typedef enum { LCE_OPT_NONE = 0, LCE_OPT_SGD = 1, LCE_OPT_ADAMW = 2 } lce_optim_kind_t;
+typedef struct {
+    lce_optim_kind_t kind;
+    float lr;
+    float weight_decay;
+    float momentum;           /* SGD */
+    float beta1, beta2, eps;  /* AdamW */
+    int64_t step;             /* 1-based number of this update */
+    float *master_W;          /* optional fp32 [V,d] master weights of a bf16 W */
+    float *exp_avg;           /* fp32 [V,d]: AdamW first moment, SGD momentum buffer */
+    float *exp_avg_sq;        /* fp32 [V,d]: AdamW second moment */
+} lce_optim_t;
+
 /* Full argument set for lce_run. Zero-initialise, then fill. */
 typedef struct {
     lce_dtype_t dtype;        /* element type of H, W and dH */
     const void *H;            /* [N,d] */
-    const void *W;            /* [V,d] */
+    const void *W;            /* [V,d]; written only by a fused optimizer step (optim) */
     const int64_t *targets;   /* [N] */
     int64_t ignore_index;
     int64_t N, d, V;
     float *loss;              /* required: device fp32 scalar */
     void *dH;                 /* [N,d] of dtype, or NULL for forward only */
-    float *dW;                /* [V,d] fp32, or NULL for forward only (NULL iff dH is NULL) */
+    float *dW;                /* [V,d] fp32, or NULL for forward only (NULL iff dH is NULL, except that
+                                 dW is NULL with a fused optimizer) */
     int accumulate_dW;        /* nonzero: dW += gradient; zero: dW = gradient */
     float grad_scale;         /* multiplies dH and dW (0 is read as 1) */
     float *lse;               /* optional [N] fp32: per-row logsumexp (natural log), NaN on ignored rows */
@@ -140,6 +180,7 @@ typedef struct {
                                  positions at a time (scratch O(token_chunk*(d + vocab_chunk)),
                                  dW accumulated across chunks in a fixed order): the chunked loss
                                  of "6GB显卡预训练11亿参数模型", section "关键参数说明" (--chunked-loss 512) */
+    const lce_optim_t *optim; /* optional: optimizer step on W fused into the backward (W is written) */
 } lce_args_t;
 
 /* Forward, or forward + backward when dH/dW are given, or backward alone

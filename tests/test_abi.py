@@ -83,7 +83,11 @@ int main(void) {{
 #define F(x) printf(" %zu", offsetof(lce_args_t, x));
   F(dtype) F(H) F(W) F(targets) F(ignore_index) F(N) F(d) F(V) F(loss) F(dH) F(dW)
   F(accumulate_dW) F(grad_scale) F(lse) F(workspace) F(workspace_bytes) F(vocab_chunk) F(stream)
-  F(lse_in) F(grad_loss) F(token_chunk)
+  F(lse_in) F(grad_loss) F(token_chunk) F(optim)
+  printf(" %zu", sizeof(lce_optim_t));
+#define G(x) printf(" %zu", offsetof(lce_optim_t, x));
+  G(kind) G(lr) G(weight_decay) G(momentum) G(beta1) G(beta2) G(eps) G(step) G(master_W) G(exp_avg)
+  G(exp_avg_sq)
   printf("\\n"); return 0; }}
 """
     with tempfile.TemporaryDirectory() as d:
@@ -94,4 +98,50 @@ int main(void) {{
         vals = [int(v) for v in subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()]
     names = [f[0] for f in _abi.LceArgs._fields_]
     assert vals[0] == ctypes.sizeof(_abi.LceArgs)
-    assert vals[1:] == [getattr(_abi.LceArgs, n).offset for n in names]
+    n = len(names)
+    assert vals[1:1 + n] == [getattr(_abi.LceArgs, k).offset for k in names]
+    onames = [f[0] for f in _abi.LceOptim._fields_]
+    assert vals[1 + n] == ctypes.sizeof(_abi.LceOptim)
+    assert vals[2 + n:] == [getattr(_abi.LceOptim, k).offset for k in onames]
+
+
+def test_fused_optimizer_option_checks_without_gpu(lib):
+    """Option combinations the fused optimizer step refuses on the host."""
+    def args(**kw):
+        a = _abi.LceArgs()
+        a.H = a.W = a.targets = a.loss = a.dH = 4096
+        a.N, a.d, a.V = 10, 64, 100
+        o = _abi.LceOptim()
+        o.kind, o.lr, o.step = _abi.LCE_OPT_ADAMW, 1e-3, 1
+        o.beta1, o.beta2, o.eps = 0.9, 0.999, 1e-8
+        o.exp_avg = o.exp_avg_sq = 8192
+        for k, v in kw.items():
+            setattr(o if hasattr(o, k) and k not in ("dW",) and not hasattr(a, k) else a, k, v)
+        a.optim = ctypes.addressof(o)
+        return a, o
+
+    def run(**kw):
+        a, o = args(**kw)
+        return lib.lce_run(ctypes.byref(a))
+
+    ok_codes = (5, 9)   # the host checks pass; there is no sm_103 device here
+    assert run() in ok_codes
+    assert run(dW=4096) == 10                       # a gradient output is never written
+    assert run(accumulate_dW=1) == 10
+    assert run(token_chunk=5) == 10                 # one token chunk only
+    assert run(token_chunk=10) in ok_codes          # a cap >= N is one chunk
+    assert run(exp_avg_sq=None) == 1                # AdamW needs both moments
+    assert run(step=0) == 10
+    assert run(beta1=1.0) == 10
+    assert run(eps=0.0) == 10
+    assert run(lr=-1.0) == 10
+    assert run(kind=7) == 10
+    assert run(kind=_abi.LCE_OPT_SGD, exp_avg=None, exp_avg_sq=None) in ok_codes
+    assert run(kind=_abi.LCE_OPT_SGD, momentum=0.9, exp_avg=None) == 1
+    assert run(master_W=8200) == 3                  # misaligned state
+    assert run(dtype=1, master_W=12288) == 10       # master weights are for bf16 W
+    assert run(dH=None) == 1                        # the update runs in the backward
+    a, _ = args()
+    a.optim = None
+    assert lib.lce_run(ctypes.byref(a)) == 1        # without an optimizer dH needs dW
+
