@@ -32,8 +32,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # from profiles/k_gemm_pair_llama8b_v24k_ncu_full.md; valid only for the
 # kernel sources it was captured from (sha256 prefix below) and the default
 # vocab chunk, else reported null.
-NCU_TRAFFIC = {"workload": "llama8b", "kernel": "backward", "bytes_per_launch": 1235.0e6,
-               "src_sha256": "13b40ec0684e0a64"}
+NCU_TRAFFIC = {"workload": "llama8b", "kernel": "backward", "bytes_per_launch": 1225.4e6,
+               "src_sha256": "1f6729f9083dec91"}
 
 
 def kernel_src_sha256() -> str:
@@ -211,6 +211,8 @@ def main():
     ap.add_argument("--vocab-chunk", type=int, default=0, help="backward vocab chunk (0 = library default)")
     ap.add_argument("--optim", default="none", choices=["none", "sgd", "adamw"],
                     help="fuse an optimizer step on W into the backward (no dW buffer; W is updated every step)")
+    ap.add_argument("--row-gather", action="store_true",
+                    help="GEMMs read H's valid rows by TMA gather4 instead of a compacted copy")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
@@ -245,17 +247,18 @@ def main():
     dH = torch.empty_like(H)
     fused = args.optim != "none"
     dW = None if fused else torch.empty(W.shape, dtype=torch.float32, device=dev)
-    ws = torch.empty(lce.workspace_size(w.N, w.d, w.V, vocab_chunk=args.vocab_chunk, fused_optimizer=fused),
-                     dtype=torch.uint8, device=dev)
+    ws = torch.empty(lce.workspace_size(w.N, w.d, w.V, vocab_chunk=args.vocab_chunk, fused_optimizer=fused,
+                                        row_gather=args.row_gather), dtype=torch.uint8, device=dev)
     opt = lce.FusedOptimizer(W, args.optim, lr=1e-5) if fused else None
 
     def run(Hx, tx, lx, dHx):
         if opt is None:
-            lce.lce_run(Hx, W, tx, -100, loss=lx, dH=dHx, dW=dW, workspace=ws, vocab_chunk=args.vocab_chunk)
+            lce.lce_run(Hx, W, tx, -100, loss=lx, dH=dHx, dW=dW, workspace=ws, vocab_chunk=args.vocab_chunk,
+                        row_gather=args.row_gather)
         else:
             opt.step_count += 1
             lce.lce_run(Hx, W, tx, -100, loss=lx, dH=dHx, workspace=ws, vocab_chunk=args.vocab_chunk,
-                        optim=opt._optim())
+                        optim=opt._optim(), row_gather=args.row_gather)
 
     def step():
         run(H, t, loss, dH)
@@ -300,7 +303,7 @@ def main():
     def e2e_step():
         H_e.copy_(H_host, non_blocking=True)
         t_e.copy_(t_host, non_blocking=True)
-        if opt is None:
+        if opt is None and not args.row_gather:
             l, _, _ = lce.lce_forward_backward(H_e, W, t_e, -100, vocab_chunk=args.vocab_chunk)
         else:
             l = torch.empty((), dtype=torch.float32, device=dev)
@@ -340,7 +343,8 @@ def main():
     achieved = flops_launch / (per_launch_ms / 1e3) / 1e12
     traffic = None
     if (NCU_TRAFFIC["workload"] == w.name and NCU_TRAFFIC["kernel"] == name and w.V == 128256
-            and NCU_TRAFFIC["src_sha256"] == kernel_src_sha256() and not args.vocab_chunk and opt is None):
+            and NCU_TRAFFIC["src_sha256"] == kernel_src_sha256() and not args.vocab_chunk and opt is None
+            and not args.row_gather):
         traffic = NCU_TRAFFIC["bytes_per_launch"]
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     total_prof = sum(p["ms"] for p in phases.values())
@@ -377,6 +381,7 @@ def main():
         "workspace_bytes": int(ws.numel()),
         "vocab_chunk": args.vocab_chunk or "library default (6144)",
         "fused_optimizer": None if opt is None else f"{args.optim} on W in place (state fp32 [V,d]; no dW buffer)",
+        "row_gather": bool(args.row_gather),
         "logits_bytes_avoided": int(w.N * w.V * 4),
     }
     print(json.dumps(line), flush=True)

@@ -74,6 +74,7 @@ class LceArgs(ctypes.Structure):
         ("grad_loss", c_void_p),
         ("token_chunk", c_int64),
         ("optim", c_void_p),
+        ("row_gather", c_int),
     ]
 
 

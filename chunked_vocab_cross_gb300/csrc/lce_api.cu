@@ -6,7 +6,10 @@
 // (all N rows unless lce_args_t.token_chunk caps it; k_count_valid first
 // counts the call's valid rows when there are several chunks):
 //   1 k_compact        valid rows -> idx / inv / Nv (device)
-//   2 k_gather         Hc = H[idx], zero-padded to 256-row pair blocks
+//   2 k_gather         Hc = H[idx], zero-padded to 256-row pair blocks (with
+//                      row_gather: no copy, the GEMMs gather H's rows by
+//                      TMA gather4; only targets and the padded index
+//                      entries are written)
 //   3 k_gemm<LSE>      logits tiles + online log-sum-exp partials + target logit
 //   4 k_lse_merge      lse per row, loss_i
 //   5 k_loss_partial   sum of loss_i (k_loss_final: loss = sum / Nv)
@@ -206,7 +209,17 @@ bool encode_map_mn3(CUtensorMap *m, const void *base, uint64_t inner, uint64_t o
 
 inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Row gather (lce_args_t.row_gather): the GEMMs read bf16 H's valid rows
+// themselves (TMA gather4 through the compaction index) instead of a
+// compacted copy Hc; only when d is a whole number of 256-column tiles, so
+// that no gather4 ever starts outside H. Off by default: on this part it is
+// several times slower than the copy kernel plus tiled loads (each gather4
+// moves 512 bytes, 32 per stage per CTA), and saves only the N_pad*d*2-byte
+// copy.
+inline bool row_gather_ok(lce_dtype_t dt, int64_t d) { return dt == LCE_BF16 && d % kBN == 0; }
+
 struct Layout {
+    bool gather = false;
     int64_t N_pad = 0, Vc = 0, part_rows = 0;
     size_t idx = 0, inv = 0, counters = 0, tc = 0, z = 0, lse2 = 0, loss_rows = 0, part = 0, Hc = 0, Hc_lo = 0,
            W_hi = 0, W_lo = 0, G = 0, G_lo = 0, dHacc = 0, gcount = 0, lpart = 0, total = 0;
@@ -216,11 +229,12 @@ struct Layout {
 // hi/lo pairs (Hc/Hc_lo, W_hi/W_lo, G/G_lo), so the fp32 path also holds a
 // split copy of W (4*V*d bytes).
 Layout make_layout(int64_t N, int64_t d, int64_t V, lce_dtype_t dt, int64_t Vc, bool backward, int n_tc = 1,
-                   int n_gbuf = kGBuffers) {
+                   int n_gbuf = kGBuffers, bool gather = false) {
     Layout L;
     const bool split = dt == LCE_FP32;
     L.N_pad = (N + kPairM - 1) / kPairM * kPairM;
     L.Vc = Vc;
+    L.gather = gather && row_gather_ok(dt, d);
     L.part_rows = lse_partial_rows(static_cast<int>(L.N_pad), kMaxSms / 2);
     size_t o = 0;
     auto take = [&](size_t bytes) {
@@ -228,7 +242,7 @@ Layout make_layout(int64_t N, int64_t d, int64_t V, lce_dtype_t dt, int64_t Vc, 
         o += up256(bytes);
         return at;
     };
-    L.idx = take(N * 4);
+    L.idx = take(L.N_pad * 4);   // padded rows get an index too (row gather)
     L.inv = take(N * 4);
     L.counters = take(64);
     L.tc = take(L.N_pad * 4);
@@ -236,7 +250,7 @@ Layout make_layout(int64_t N, int64_t d, int64_t V, lce_dtype_t dt, int64_t Vc, 
     L.lse2 = take(L.N_pad * 4);
     L.loss_rows = take(L.N_pad * 4);
     L.part = take(L.part_rows * 8);
-    L.Hc = take(L.N_pad * d * 2);
+    if (!L.gather) L.Hc = take(L.N_pad * d * 2);
     if (split) {
         L.Hc_lo = take(L.N_pad * d * 2);
         L.W_hi = take(static_cast<size_t>(V) * d * 2);
@@ -276,6 +290,7 @@ lce_status_t check_args(const lce_args_t *a) {
         a->vocab_chunk > (int64_t(1) << 20) || a->token_chunk < 0)
         return LCE_ERR_SHAPE;
     if (a->d % 8) return LCE_ERR_ALIGN;   // bf16 rows (operands or their split copies) of 16-byte multiples
+    if (a->row_gather && !row_gather_ok(a->dtype, a->d)) return LCE_ERR_ARG;
     auto mis = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
     if (mis(a->H) || mis(a->W) || (a->dH && mis(a->dH)) || (a->dW && mis(a->dW)) ||
         (a->workspace && mis(a->workspace)))
@@ -351,7 +366,7 @@ lce_status_t run_rows(const lce_args_t *a, const DevInfo &di, uint8_t *base, con
     float *lse2 = reinterpret_cast<float *>(base + L.lse2);
     float *loss_rows = reinterpret_cast<float *>(base + L.loss_rows);
     float2 *part = reinterpret_cast<float2 *>(base + L.part);
-    __nv_bfloat16 *Hc = bf(L.Hc);
+    __nv_bfloat16 *Hc = L.gather ? nullptr : bf(L.Hc);
     __nv_bfloat16 *Hc_lo = split ? bf(L.Hc_lo) : nullptr;
     const __nv_bfloat16 *W_hi = split ? bf(L.W_hi) : static_cast<const __nv_bfloat16 *>(a->W);
     const __nv_bfloat16 *W_lo = split ? bf(L.W_lo) : W_hi;
@@ -359,14 +374,23 @@ lce_status_t run_rows(const lce_args_t *a, const DevInfo &di, uint8_t *base, con
     __nv_bfloat16 *G_lo = backward && split ? bf(L.G_lo) : G;
     float *dHacc = backward ? reinterpret_cast<float *>(base + L.dHacc) : nullptr;
     const __nv_bfloat16 *Hc_lo_or_hi = split ? Hc_lo : Hc;
+    // row gather: one map over the caller's H with a one-row box
+    CUtensorMap h_rows;
+    memset(&h_rows, 0, sizeof(h_rows));
+    if (L.gather && !encode_map(&h_rows, a->H, d, N, kBK, 1)) return LCE_ERR_CUDA;
 
     // K-major operand maps (box 64 x rows) and MN-major ones (box 64 x 64)
     GemmMaps maps_lse;
     memset(&maps_lse, 0, sizeof(maps_lse));
     {
         OperandMaps &o = maps_lse.t[map_slot(T_LSE)];
-        if (!encode_map(&o.A[0], Hc, d, L.N_pad, kBK, kBM) || !encode_map(&o.A[1], Hc_lo_or_hi, d, L.N_pad, kBK, kBM) ||
-            !encode_map(&o.B[0], W_hi, d, V, kBK, kHalfN) || !encode_map(&o.B[1], W_lo, d, V, kBK, kHalfN))
+        if (L.gather) {
+            o.A[0] = o.A[1] = h_rows;
+        } else if (!encode_map(&o.A[0], Hc, d, L.N_pad, kBK, kBM) ||
+                   !encode_map(&o.A[1], Hc_lo_or_hi, d, L.N_pad, kBK, kBM)) {
+            return LCE_ERR_CUDA;
+        }
+        if (!encode_map(&o.B[0], W_hi, d, V, kBK, kHalfN) || !encode_map(&o.B[1], W_lo, d, V, kBK, kHalfN))
             return LCE_ERR_CUDA;
     }
 
@@ -380,6 +404,8 @@ lce_status_t run_rows(const lce_args_t *a, const DevInfo &di, uint8_t *base, con
     ga.num_pairs = pairs;
     ga.nseg = split ? 3 : 1;
     ga.tc = tc;
+    ga.gather = L.gather ? 1 : 0;
+    ga.idx = idx;
     ga.grad_scale = a->grad_scale == 0.f ? 1.f : a->grad_scale;
     ga.grad_ptr = a->grad_loss;
     const int n_tiles_v = cdiv(V, kBN);
@@ -451,7 +477,12 @@ lce_status_t run_rows(const lce_args_t *a, const DevInfo &di, uint8_t *base, con
             !encode_map_mn3(&dw.A[0], Gb, Vc, L.N_pad, kBK, kBM / kAtom) ||
             !encode_map_mn3(&dw.A[1], Gb_lo, Vc, L.N_pad, kBK, kBM / kAtom))
             return LCE_ERR_CUDA;
-        if (mn3d_d) {
+        if (L.gather) {
+            if (!encode_map_mn3(&dh.B[0], W_hi, d, V, kBK, kHalfN / kAtom) ||
+                !encode_map_mn3(&dh.B[1], W_lo, d, V, kBK, kHalfN / kAtom))
+                return LCE_ERR_CUDA;
+            dw.B[0] = dw.B[1] = h_rows;
+        } else if (mn3d_d) {
             if (!encode_map_mn3(&dh.B[0], W_hi, d, V, kBK, kHalfN / kAtom) ||
                 !encode_map_mn3(&dh.B[1], W_lo, d, V, kBK, kHalfN / kAtom) ||
                 !encode_map_mn3(&dw.B[0], Hc, d, L.N_pad, kBK, kHalfN / kAtom) ||
@@ -574,7 +605,7 @@ lce_status_t run_typed(const lce_args_t *a, const DevInfo &di) {
     const int64_t C = token_rows(a->N, a->token_chunk);
     const int n_tc = static_cast<int>((a->N + C - 1) / C);
     const Layout L = make_layout(C, a->d, a->V, a->dtype, Vc, backward, n_tc,
-                                 has_optim(a) ? kGBuffersOpt : kGBuffers);
+                                 has_optim(a) ? kGBuffersOpt : kGBuffers, a->row_gather != 0);
 
     WsGuard ws;
     ws.s = st;
@@ -768,7 +799,7 @@ size_t lce_workspace_size_args(const lce_args_t *a) {
     const int64_t C = token_rows(a->N, a->token_chunk);
     const int n_tc = static_cast<int>((a->N + C - 1) / C);
     return make_layout(C, a->d, a->V, a->dtype, pick_chunk(a->V, a->vocab_chunk), a->dH != nullptr, n_tc,
-                       has_optim(a) ? kGBuffersOpt : kGBuffers)
+                       has_optim(a) ? kGBuffersOpt : kGBuffers, a->row_gather != 0)
         .total;
 }
 

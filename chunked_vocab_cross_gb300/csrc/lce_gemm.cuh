@@ -29,6 +29,12 @@
 //   T_DH   dHacc (+)= G . W_c (M = valid tokens, K = chunk vocab rows); B is
 //          read MN-major straight from W.
 //
+// Row gather (optional; bf16 inputs, d a multiple of 256): instead of a
+// compacted copy Hc, the producer warp loads the valid rows of H itself, each
+// lane one tile::gather4 of four rows x 128 bytes per stage (32 lanes: the 128
+// rows of a K-major A block, or 64 token rows x 2 column blocks of an MN-major
+// B), with row numbers from the compaction index.
+//
 // Split precision (fp32 inputs): every fp32 operand x is carried as two bf16
 // tensors, x = hi + lo with hi = bf16(x) and lo = bf16(x - hi), and the K loop
 // runs three segments, A_hi.B_hi + A_hi.B_lo + A_lo.B_hi, into the same
@@ -185,6 +191,12 @@ struct GemmArgs {
     // (one {64, 64} box per column block); 3-D needs the MN extent to be a
     // multiple of 64. Bit 0: DW's A (G), bit 1: DW's B (Hc), bit 2: DH's B (W).
     int mn3d;
+    // Row gather: the Hc operand (A of LSE / G tiles, B of DW tiles) is read
+    // straight from the caller's bf16 H through the compaction index, rows
+    // idx[r] (padded rows repeat a valid row; their G rows are zero), by
+    // tile::gather4 loads; the operand map is then a {64, 1}-box map of H.
+    int gather;
+    const int *idx;
     OptArgs opt;
 };
 
@@ -425,6 +437,98 @@ __device__ __forceinline__ void load_operands(const TileInfo &t, const GemmArgs 
     }
 }
 
+// TMA producer of one CTA: waits for free stages and issues this CTA's loads
+// of every k-block of its tiles, completing on the even CTA's full barrier.
+// kGather = false runs on one thread (lane 0): the producer's reaction time
+// per stage is on the MMA's critical path, so no warp-wide step is taken.
+// kGather = true runs on the whole warp: lane 0 waits and issues the tiled
+// loads, and every lane issues one tile::gather4 of the gathered operand.
+template <int KIND, bool kGather>
+__device__ __forceinline__ void producer(const GemmMaps &maps, const GemmArgs &a, const Sched &s, int pair,
+                                         int npairs, uint32_t rank, int lane, uint8_t *smem, uint64_t *full,
+                                         uint64_t *empty, uint32_t full_even, volatile int *abort_flag) {
+    int it = 0;
+    bool ok = true;
+    bool dep_done = false;
+    const int arow = static_cast<int>(rank) * kBM;      // this CTA's A rows within the pair tile
+    const int brow = static_cast<int>(rank) * kHalfN;   // this CTA's B rows (N) within the tile
+    const int4 *idx4 = reinterpret_cast<const int4 *>(a.idx);
+    for (int u = pair; ok && u < s.units; u += npairs) {
+        int n0, n1;
+        unit_range<KIND>(s, u, n0, n1);
+        for (int n = n0; ok && n < n1; ++n) {
+            const TileInfo t = tile_info<KIND>(s, u, n);
+            if (KIND != KIND_LSE && !dep_done && t.type != T_G) {
+                // dW / dH read what the previous launch wrote; every thread
+                // that issues loads waits
+                griddep_wait();
+                if (lane == 0) griddep_launch_dependents();
+                dep_done = true;
+            }
+            const OperandMaps &om = maps.t[map_slot(t.type)];
+            const int k_blocks = t.kseg * a.nseg;
+            const int am = t.mb * kPairM + arow;   // first A row (M) of this CTA
+            const int bn = t.nt * kBN + brow;      // first B row (N) of this CTA
+            const bool gA = kGather && (t.type == T_LSE || t.type == T_G);
+            const bool gB = kGather && t.type == T_DW;
+            int4 rows = make_int4(0, 0, 0, 0);     // this lane's four gathered rows
+            if (gA) rows = idx4[(am >> 2) + lane];
+            int4 rows_next = rows;
+            if (gB && k_blocks > 0) rows_next = idx4[(lane & 15)];
+            for (int kbt = 0; kbt < k_blocks; ++kbt, ++it) {
+                const int st = it % kStages;
+                if (gB) {
+                    // token rows of this k-block; the next block's are fetched
+                    // before the wait so that their latency overlaps it
+                    rows = rows_next;
+                    if (kbt + 1 < k_blocks) rows_next = idx4[(((kbt + 1) * kBK) >> 2) + (lane & 15)];
+                }
+                if (kGather) {
+                    bool got = true;
+                    if (lane == 0) got = wait_bar(&empty[st], ((it / kStages) & 1) ^ 1, abort_flag);
+                    if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+                        ok = false;
+                        break;
+                    }
+                } else if (!wait_bar(&empty[st], ((it / kStages) & 1) ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                // segment 0: hi.hi, 1: hi.lo, 2: lo.hi
+                const int seg = kbt / t.kseg;
+                const int k0 = (kbt - seg * t.kseg) * kBK;
+                const CUtensorMap *ma = &om.A[seg == 2 ? 1 : 0];
+                const CUtensorMap *mbp = &om.B[seg == 1 ? 1 : 0];
+                if (rank == 0 && lane == 0) mbar_arrive_expect_tx(&full[st], kPairTx);
+                const uint32_t fb = full_even + st * 8;
+                uint8_t *sa = smem + st * kStageBytes;
+                uint8_t *sb = sa + kStageA;
+                if (gA) {
+                    tma_gather4_pair(sa + lane * 512, ma, fb, k0, rows);
+                    if (lane == 0) tma_load_2d_pair(sb, mbp, fb, k0, (t.type == T_G ? a.v0n : 0) + bn);
+                } else if (gB) {
+                    // lanes 0-15: column block 0, lanes 16-31: block 1; 4 token rows each
+                    tma_gather4_pair(sb + (lane >> 4) * kAtomBytes + (lane & 15) * 512, mbp, fb,
+                                     bn + (lane >> 4) * kAtom, rows);
+                    if (lane == 0) tma_load_3d_pair(sa, ma, fb, 0, k0, am / kAtom);
+                } else if (lane == 0) {
+                    load_operands(t, a, ma, mbp, sa, sb, fb, am, bn, k0);
+                }
+            }
+        }
+    }
+    if (KIND != KIND_LSE && !dep_done) {
+        // the next launch may only start once the one before this has finished
+        griddep_wait();
+        if (lane == 0) griddep_launch_dependents();
+    }
+    if (!ok && rank == 0 && lane == 0) {
+        // let the copies already issued (by both CTAs) land before the pair exits
+        const int first = it > kStages ? it - kStages : 0;
+        for (int j = first; j < it; ++j) drain_bar(&full[j % kStages], (j / kStages) & 1);
+    }
+}
+
 // One CTA pair (cluster of 2) per two SMs. Each CTA loads its 128 A rows and
 // its 128 of the 256 B rows per stage; the even CTA waits for both halves on
 // its full barrier, issues tcgen05.mma.cta_group::2 (M = 256, N = 256) and
@@ -492,57 +596,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------- TMA producer
-        if (lane == 0) {
-            int it = 0;
-            bool ok = true;
-            bool dep_done = false;
-            const int arow = static_cast<int>(rank) * kBM;      // this CTA's A rows within the pair tile
-            const int brow = static_cast<int>(rank) * kHalfN;   // this CTA's B rows (N) within the tile
-            for (int u = pair; ok && u < s.units; u += npairs) {
-                int n0, n1;
-                unit_range<KIND>(s, u, n0, n1);
-                for (int n = n0; ok && n < n1; ++n) {
-                    const TileInfo t = tile_info<KIND>(s, u, n);
-                    if (KIND != KIND_LSE && !dep_done && t.type != T_G) {
-                        // dW / dH read what the previous launch wrote
-                        griddep_wait();
-                        griddep_launch_dependents();
-                        dep_done = true;
-                    }
-                    const OperandMaps &om = maps.t[map_slot(t.type)];
-                    const int k_blocks = t.kseg * a.nseg;
-                    for (int kbt = 0; kbt < k_blocks; ++kbt, ++it) {
-                        const int st = it % kStages;
-                        if (!wait_bar(&empty[st], ((it / kStages) & 1) ^ 1, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        // segment 0: hi.hi, 1: hi.lo, 2: lo.hi
-                        const int seg = kbt / t.kseg;
-                        const int k0 = (kbt - seg * t.kseg) * kBK;
-                        const CUtensorMap *ma = &om.A[seg == 2 ? 1 : 0];
-                        const CUtensorMap *mbp = &om.B[seg == 1 ? 1 : 0];
-                        if (rank == 0) mbar_arrive_expect_tx(&full[st], kPairTx);
-                        const uint32_t fb = full_even + st * 8;
-                        uint8_t *sa = smem + st * kStageBytes;
-                        uint8_t *sb = sa + kStageA;
-                        const int am = t.mb * kPairM + arow;   // first A row (M) of this CTA
-                        const int bn = t.nt * kBN + brow;      // first B row (N) of this CTA
-                        load_operands(t, a, ma, mbp, sa, sb, fb, am, bn, k0);
-                    }
-                }
-            }
-            if (KIND != KIND_LSE && !dep_done) {
-                // the next launch may only start once the one before this has finished
-                griddep_wait();
-                griddep_launch_dependents();
-            }
-            if (!ok && rank == 0) {
-                // let the copies already issued (by both CTAs) land before the pair exits
-                const int first = it > kStages ? it - kStages : 0;
-                for (int j = first; j < it; ++j) drain_bar(&full[j % kStages], (j / kStages) & 1);
-            }
-        }
+        // lane 0 alone, except with row gather, where every lane issues one
+        // gather4 per stage
+        if (a.gather)
+            producer<KIND, true>(maps, a, s, pair, npairs, rank, lane, smem, full, empty, full_even, abort_flag);
+        else if (lane == 0)
+            producer<KIND, false>(maps, a, s, pair, npairs, rank, lane, smem, full, empty, full_even, abort_flag);
     } else if (warp == 1) {
         // ------------------------------------------- MMA issue (even CTA only)
         if (lane == 0 && rank == 0) {

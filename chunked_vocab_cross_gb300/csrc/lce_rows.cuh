@@ -71,7 +71,10 @@ __global__ void __launch_bounds__(kCompactThreads)
 // Hc[r] = H[idx[r]] for r < Nv, zero rows on [Nv, round_up(Nv, 256)) so the
 // tensor-core passes can read whole 256-row pair blocks; tc[r] = target (or -1),
 // z[r] = NaN until the logits pass finds the target column. bf16 rows are
-// copied; fp32 rows are split into bf16 hi and lo parts (Hc, Hc_lo).
+// copied; fp32 rows are split into bf16 hi and lo parts (Hc, Hc_lo). With
+// Hc == nullptr the GEMMs gather H's rows themselves: no rows are copied and
+// idx[r] for the padded rows r in [Nv, round_up(Nv, 256)) is set to idx[0], a
+// valid row (finite values; the padded rows' softmax gradient is zero).
 __device__ __forceinline__ void gather8(const __nv_bfloat16 *src, __nv_bfloat16 *hi, __nv_bfloat16 *, bool live) {
     *reinterpret_cast<uint4 *>(hi) = live ? *reinterpret_cast<const uint4 *>(src) : make_uint4(0, 0, 0, 0);
 }
@@ -95,7 +98,7 @@ __device__ __forceinline__ void gather8(const float *src, __nv_bfloat16 *hi, __n
 
 template <typename T>
 __global__ void __launch_bounds__(256)
-    k_gather(const T *__restrict__ H, const int64_t *__restrict__ t, int d, int64_t V, const int *__restrict__ idx,
+    k_gather(const T *__restrict__ H, const int64_t *__restrict__ t, int d, int64_t V, int *__restrict__ idx,
              const int *__restrict__ counters, __nv_bfloat16 *__restrict__ Hc, __nv_bfloat16 *__restrict__ Hc_lo,
              int *__restrict__ tc, float *__restrict__ z) {
     const int nv = counters[0];
@@ -104,10 +107,15 @@ __global__ void __launch_bounds__(256)
     for (int r = blockIdx.x; r < rows; r += gridDim.x) {
         const bool live = r < nv;
         const int src_row = live ? idx[r] : 0;
-        const T *src = H + static_cast<size_t>(src_row) * d;
-        __nv_bfloat16 *hi = Hc + static_cast<size_t>(r) * d;
-        __nv_bfloat16 *lo = Hc_lo ? Hc_lo + static_cast<size_t>(r) * d : nullptr;
-        for (int g = threadIdx.x; g < groups; g += blockDim.x) gather8(src + 8 * g, hi + 8 * g, lo ? lo + 8 * g : nullptr, live);
+        if (Hc) {
+            const T *src = H + static_cast<size_t>(src_row) * d;
+            __nv_bfloat16 *hi = Hc + static_cast<size_t>(r) * d;
+            __nv_bfloat16 *lo = Hc_lo ? Hc_lo + static_cast<size_t>(r) * d : nullptr;
+            for (int g = threadIdx.x; g < groups; g += blockDim.x)
+                gather8(src + 8 * g, hi + 8 * g, lo ? lo + 8 * g : nullptr, live);
+        } else if (!live && threadIdx.x == 0) {
+            idx[r] = idx[0];
+        }
         if (threadIdx.x == 0) {
             const int64_t tt = live ? t[src_row] : -1;
             tc[r] = (tt >= 0 && tt < V) ? static_cast<int>(tt) : -1;

@@ -159,6 +159,19 @@ __device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *m
         : "memory");
 }
 
+// Row gather (tile::gather4): four rows r.x..r.w of a 2-D map whose box is one
+// row high, each box-width elements from column x, landing as four
+// consecutive rows at dst (swizzled like a tiled load); pair form as above.
+__device__ __forceinline__ void tma_gather4_pair(void *dst, const CUtensorMap *m, uint32_t bar_cluster, int x,
+                                                 int4 r) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(x), "r"(r.x), "r"(r.y),
+          "r"(r.z), "r"(r.w)
+        : "memory");
+}
+
 // ------------------------------------------------------------------- tcgen05
 
 __device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {

@@ -32,12 +32,13 @@ def _check_inputs(H: torch.Tensor, W: torch.Tensor, targets: torch.Tensor):
 
 
 def workspace_size(N: int, d: int, V: int, dtype=torch.bfloat16, vocab_chunk: int = 0, token_chunk: int = 0,
-                   backward: bool = True, fused_optimizer: bool = False) -> int:
+                   backward: bool = True, fused_optimizer: bool = False, row_gather: bool = False) -> int:
     a = _abi.LceArgs()
     a.dtype = _DT[dtype]
     a.N, a.d, a.V = N, d, V
     a.vocab_chunk, a.token_chunk = vocab_chunk, token_chunk
     a.dH = 1 if backward else None      # only whether gradients are wanted matters
+    a.row_gather = 1 if row_gather else 0
     o = _abi.LceOptim()
     if fused_optimizer:
         o.kind = _abi.LCE_OPT_SGD
@@ -47,7 +48,7 @@ def workspace_size(N: int, d: int, V: int, dtype=torch.bfloat16, vocab_chunk: in
 
 def lce_run(H, W, targets, ignore_index: int = -100, *, loss=None, dH=None, dW=None, accumulate_dW: bool = False,
             grad_scale: float = 1.0, lse=None, workspace=None, vocab_chunk: int = 0, lse_in=None, grad_loss=None,
-            token_chunk: int = 0, optim=None, stream=None) -> None:
+            token_chunk: int = 0, optim=None, row_gather: bool = False, stream=None) -> None:
     """Raw lce_run over caller-provided output tensors. `optim` is an
     _abi.LceOptim (a fused optimizer step on W) or None."""
     _check_inputs(H, W, targets)
@@ -71,6 +72,7 @@ def lce_run(H, W, targets, ignore_index: int = -100, *, loss=None, dH=None, dW=N
     a.vocab_chunk = int(vocab_chunk)
     a.token_chunk = int(token_chunk)
     a.optim = ctypes.addressof(optim) if optim is not None else None
+    a.row_gather = 1 if row_gather else 0
     a.stream = _stream(stream)
     _abi.check(_abi.lib().lce_run(ctypes.byref(a)), "lce_run")
 

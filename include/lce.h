@@ -181,6 +181,13 @@ typedef struct {
                                  dW accumulated across chunks in a fixed order): the chunked loss
                                  of "6GB显卡预训练11亿参数模型", section "关键参数说明" (--chunked-loss 512) */
     const lce_optim_t *optim; /* optional: optimizer step on W fused into the backward (W is written) */
+    int row_gather;           /* nonzero: the GEMMs read H's valid rows through the compaction index
+                                 with TMA gather4 loads instead of from a compacted copy (no
+                                 N*d*2-byte copy in the workspace; bf16 and d % 256 == 0 only, else
+                                 LCE_ERR_ARG). Same results; slower on sm_103 (32 gather4 of 512
+                                 bytes per pipeline stage against one tiled load). The dense index
+                                 list of "为什么26万词表会卡死16GB显卡", section 2.3 稀疏索引引擎,
+                                 used directly as the operand's row map. */
 } lce_args_t;
 
 /* Forward, or forward + backward when dH/dW are given, or backward alone

@@ -83,7 +83,7 @@ int main(void) {{
 #define F(x) printf(" %zu", offsetof(lce_args_t, x));
   F(dtype) F(H) F(W) F(targets) F(ignore_index) F(N) F(d) F(V) F(loss) F(dH) F(dW)
   F(accumulate_dW) F(grad_scale) F(lse) F(workspace) F(workspace_bytes) F(vocab_chunk) F(stream)
-  F(lse_in) F(grad_loss) F(token_chunk) F(optim)
+  F(lse_in) F(grad_loss) F(token_chunk) F(optim) F(row_gather)
   printf(" %zu", sizeof(lce_optim_t));
 #define G(x) printf(" %zu", offsetof(lce_optim_t, x));
   G(kind) G(lr) G(weight_decay) G(momentum) G(beta1) G(beta2) G(eps) G(step) G(master_W) G(exp_avg)
@@ -145,3 +145,21 @@ def test_fused_optimizer_option_checks_without_gpu(lib):
     a.optim = None
     assert lib.lce_run(ctypes.byref(a)) == 1        # without an optimizer dH needs dW
 
+
+
+def test_row_gather_option_checks_without_gpu(lib):
+    a = _abi.LceArgs()
+    a.H = a.W = a.targets = a.loss = 4096
+    a.N, a.d, a.V = 10, 512, 100
+    a.row_gather = 1
+    assert lib.lce_run(ctypes.byref(a)) in (5, 9)     # accepted (no sm_103 device here)
+    a.d = 320
+    assert lib.lce_run(ctypes.byref(a)) == 10         # d not a multiple of 256
+    a.d, a.dtype = 512, 1
+    assert lib.lce_run(ctypes.byref(a)) == 10         # fp32 inputs are split, not gathered
+    # the gathered operand needs no compacted copy: N_pad * d * 2 bytes less workspace
+    b = _abi.LceArgs()
+    b.N, b.d, b.V, b.dH = 1000, 512, 5000, 4096
+    full = lib.lce_workspace_size_args(ctypes.byref(b))
+    b.row_gather = 1
+    assert full - lib.lce_workspace_size_args(ctypes.byref(b)) == 1024 * 512 * 2

@@ -418,3 +418,54 @@ def test_bounded_wait_times_out_into_the_status_word():
     assert lce.device_status() == 0      # reading clears the word
     x = make_inputs("gpt1b", N=300, d=128, V=1000, padding=("random_frac", 0.1), seqs=1)
     _run_and_compare(x)
+
+
+@pytest.mark.parametrize("nv", [0, 1, 255, 256, 257, 511])
+def test_row_gather_ragged_valid_counts(nv):
+    """row_gather: the GEMMs gather H's valid rows by TMA gather4 through the
+    compaction index (no compacted copy). Valid counts around the 256-row pair
+    blocks, valid rows scattered over the batch; results equal to the oracle
+    and bitwise equal to the default (copy) path."""
+    import dataclasses
+    x = make_inputs("gpt1b", N=700, d=256, V=1500, padding=("none",), seqs=1)
+    g = np.random.default_rng(nv)
+    t = np.full(700, IGNORE_INDEX, dtype=np.int64)
+    pos = np.sort(g.choice(700, nv, replace=False))
+    t[pos] = g.integers(0, 1500, nv)
+    x = dataclasses.replace(x, targets=t)
+    H, W, tt = to_device(x)
+    outs = []
+    for rg in (True, False):
+        loss = torch.empty((), dtype=torch.float32, device="cuda")
+        dH, dW = torch.empty_like(H), torch.empty(W.shape, dtype=torch.float32, device="cuda")
+        lse = torch.empty(700, dtype=torch.float32, device="cuda")
+        lce.lce_run(H, W, tt, IGNORE_INDEX, loss=loss, dH=dH, dW=dW, lse=lse, vocab_chunk=768, row_gather=rg)
+        torch.cuda.synchronize()
+        assert lce.device_status() == 0
+        outs.append((loss, dH, dW))
+    (loss, dH, dW), (loss_c, dH_c, dW_c) = outs
+    assert torch.equal(dH, dH_c) and torch.equal(dW, dW_c)
+    if nv == 0:
+        assert math.isnan(loss.item()) and torch.count_nonzero(dH).item() == 0 and torch.count_nonzero(dW).item() == 0
+        return
+    assert torch.equal(loss, loss_c)
+    ref = oracle.forward_backward(x.H_f32(), x.W_f32(), x.targets, IGNORE_INDEX)
+    assert abs(loss.item() - ref["loss"]) <= TOL_LOSS
+    assert rel_fro(np64(dH), ref["dH"]) <= TOL_REL and rel_fro(np64(dW), ref["dW"]) <= TOL_REL
+
+
+def test_row_gather_gpt1b_shape_bitwise_equal_to_copy_path():
+    """Full gpt1b shape: the gathered-row call gives the copy path's loss, dH
+    and dW bit for bit (the same bf16 values reach the same MMAs)."""
+    x = make_inputs("gpt1b")
+    H, W, t = to_device(x)
+    outs = []
+    for rg in (True, False):
+        loss = torch.empty((), dtype=torch.float32, device="cuda")
+        dH, dW = torch.empty_like(H), torch.empty(W.shape, dtype=torch.float32, device="cuda")
+        lce.lce_run(H, W, t, IGNORE_INDEX, loss=loss, dH=dH, dW=dW, row_gather=rg)
+        torch.cuda.synchronize()
+        assert lce.device_status() == 0
+        outs.append((loss, dH, dW))
+    for a_, b_ in zip(*outs):
+        assert torch.equal(a_, b_)
