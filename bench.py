@@ -197,6 +197,49 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def eager_context(H, W, t, nv, steps):
+    """Context only (not a baseline of this metric's reference arm): the same
+    fwd+bwd in eager PyTorch, which materialises the N x V logits (cuBLAS bf16
+    GEMMs, F.cross_entropy over fp32 logits, autograd). Time per step with
+    CUDA events and the peak device memory it adds; None if it does not fit."""
+    import torch
+    import torch.nn.functional as F
+    Hr = H.detach().clone().requires_grad_(True)
+    Wr = W.detach().clone().requires_grad_(True)
+
+    def step():
+        Hr.grad = None
+        Wr.grad = None
+        loss = F.cross_entropy((Hr @ Wr.t()).float(), t, ignore_index=-100)
+        loss.backward()
+        return loss
+
+    try:
+        torch.cuda.synchronize()
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize()
+        base = torch.cuda.memory_allocated()
+        torch.cuda.reset_peak_memory_stats()
+        n = max(3, min(steps, 10))
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for _ in range(n):
+            step()
+        s1.record()
+        torch.cuda.synchronize()
+        ms = s0.elapsed_time(s1) / n
+        peak = torch.cuda.max_memory_allocated() - base
+    except torch.cuda.OutOfMemoryError:
+        return None
+    finally:
+        del Hr, Wr
+        torch.cuda.empty_cache()
+    return {"ms_per_step": ms, "valid_tokens_per_s": nv / (ms / 1e3), "peak_extra_bytes": int(peak),
+            "what": "eager PyTorch: H @ W^T (bf16 cuBLAS), F.cross_entropy on fp32 logits, autograd; "
+                    "materialises N x V logits; context, not this path"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -211,6 +254,8 @@ def main():
     ap.add_argument("--vocab-chunk", type=int, default=0, help="backward vocab chunk (0 = library default)")
     ap.add_argument("--optim", default="none", choices=["none", "sgd", "adamw"],
                     help="fuse an optimizer step on W into the backward (no dW buffer; W is updated every step)")
+    ap.add_argument("--no-context", action="store_true",
+                    help="skip the eager PyTorch context measurement (logits materialised)")
     ap.add_argument("--row-gather", action="store_true",
                     help="GEMMs read H's valid rows by TMA gather4 instead of a compacted copy")
     args = ap.parse_args()
@@ -328,6 +373,8 @@ def main():
             dist.destroy_process_group()
         return
 
+    context = None if args.no_context else eager_context(H, W, t, nv, args.steps)
+
     peaks, peak_src = load_peaks()
     useful_flops = 6.0 * nv * w.d * w.V
     executed_flops = 8.0 * nv * w.d * w.V
@@ -383,6 +430,7 @@ def main():
         "fused_optimizer": None if opt is None else f"{args.optim} on W in place (state fp32 [V,d]; no dW buffer)",
         "row_gather": bool(args.row_gather),
         "logits_bytes_avoided": int(w.N * w.V * 4),
+        "context_torch_eager": context,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
