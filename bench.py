@@ -254,6 +254,10 @@ def main():
     ap.add_argument("--vocab-chunk", type=int, default=0, help="backward vocab chunk (0 = library default)")
     ap.add_argument("--optim", default="none", choices=["none", "sgd", "adamw"],
                     help="fuse an optimizer step on W into the backward (no dW buffer; W is updated every step)")
+    ap.add_argument("--two-call", action="store_true",
+                    help="forward (storing the per-row lse) and backward from the stored lse as two calls")
+    ap.add_argument("--token-chunk", type=int, default=0,
+                    help="process the rows this many positions at a time (0 = all at once)")
     ap.add_argument("--no-context", action="store_true",
                     help="skip the eager PyTorch context measurement (logits materialised)")
     ap.add_argument("--row-gather", action="store_true",
@@ -292,18 +296,24 @@ def main():
     dH = torch.empty_like(H)
     fused = args.optim != "none"
     dW = None if fused else torch.empty(W.shape, dtype=torch.float32, device=dev)
-    ws = torch.empty(lce.workspace_size(w.N, w.d, w.V, vocab_chunk=args.vocab_chunk, fused_optimizer=fused,
-                                        row_gather=args.row_gather), dtype=torch.uint8, device=dev)
+    ws = torch.empty(lce.workspace_size(w.N, w.d, w.V, vocab_chunk=args.vocab_chunk, token_chunk=args.token_chunk,
+                                        fused_optimizer=fused, row_gather=args.row_gather),
+                     dtype=torch.uint8, device=dev)
+    lse_buf = torch.empty(w.N, dtype=torch.float32, device=dev) if args.two_call else None
     opt = lce.FusedOptimizer(W, args.optim, lr=1e-5) if fused else None
 
     def run(Hx, tx, lx, dHx):
-        if opt is None:
-            lce.lce_run(Hx, W, tx, -100, loss=lx, dH=dHx, dW=dW, workspace=ws, vocab_chunk=args.vocab_chunk,
-                        row_gather=args.row_gather)
-        else:
+        kw = dict(workspace=ws, vocab_chunk=args.vocab_chunk, token_chunk=args.token_chunk,
+                  row_gather=args.row_gather)
+        if opt is not None:
             opt.step_count += 1
-            lce.lce_run(Hx, W, tx, -100, loss=lx, dH=dHx, workspace=ws, vocab_chunk=args.vocab_chunk,
-                        optim=opt._optim(), row_gather=args.row_gather)
+            kw["optim"] = opt._optim()
+        if args.two_call:
+            # forward storing lse, then the backward alone from it
+            lce.lce_run(Hx, W, tx, -100, loss=lx, lse=lse_buf, **kw)
+            lce.lce_run(Hx, W, tx, -100, dH=dHx, dW=dW, lse_in=lse_buf, **kw)
+        else:
+            lce.lce_run(Hx, W, tx, -100, loss=lx, dH=dHx, dW=dW, **kw)
 
     def step():
         run(H, t, loss, dH)
@@ -348,7 +358,7 @@ def main():
     def e2e_step():
         H_e.copy_(H_host, non_blocking=True)
         t_e.copy_(t_host, non_blocking=True)
-        if opt is None and not args.row_gather:
+        if opt is None and not (args.row_gather or args.two_call or args.token_chunk):
             l, _, _ = lce.lce_forward_backward(H_e, W, t_e, -100, vocab_chunk=args.vocab_chunk)
         else:
             l = torch.empty((), dtype=torch.float32, device=dev)
@@ -391,7 +401,7 @@ def main():
     traffic = None
     if (NCU_TRAFFIC["workload"] == w.name and NCU_TRAFFIC["kernel"] == name and w.V == 128256
             and NCU_TRAFFIC["src_sha256"] == kernel_src_sha256() and not args.vocab_chunk and opt is None
-            and not args.row_gather):
+            and not (args.row_gather or args.two_call or args.token_chunk)):
         traffic = NCU_TRAFFIC["bytes_per_launch"]
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     total_prof = sum(p["ms"] for p in phases.values())
@@ -429,6 +439,8 @@ def main():
         "vocab_chunk": args.vocab_chunk or "library default (6144)",
         "fused_optimizer": None if opt is None else f"{args.optim} on W in place (state fp32 [V,d]; no dW buffer)",
         "row_gather": bool(args.row_gather),
+        "two_call": bool(args.two_call),
+        "token_chunk": args.token_chunk or None,
         "logits_bytes_avoided": int(w.N * w.V * 4),
         "context_torch_eager": context,
     }
