@@ -205,6 +205,22 @@ bool encode_map_mn3(CUtensorMap *m, const void *base, uint64_t inner, uint64_t o
     return r == CUDA_SUCCESS;
 }
 
+// Fused-optimizer boxes {16, 32} over a row-major [V][d] array: fp32 with
+// 64-byte swizzle, or bf16 with 32-byte swizzle (the layouts the optimizer
+// epilogue reads and writes).
+bool encode_opt_map(CUtensorMap *m, const void *base, bool fp32, uint64_t d, uint64_t V) {
+    const uint64_t elt = fp32 ? 4 : 2;
+    cuuint64_t dims[2] = {d, V};
+    cuuint64_t strides[1] = {d * elt};
+    cuuint32_t box[2] = {16, 32};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = g_encode(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                          const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          fp32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // ----------------------------------------------------------------- workspace
 
 inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -504,8 +520,17 @@ lce_status_t run_rows(const lce_args_t *a, const DevInfo &di, uint8_t *base, con
         return LCE_ERR_CUDA;
 
     OptArgs oa{};
+    CUtensorMap opt_maps[4];   // m, v, fp32 weights, bf16 W
+    memset(opt_maps, 0, sizeof(opt_maps));
     if (opt) {
         const lce_optim_t *o = a->optim;
+        const bool use_m = o->kind == LCE_OPT_ADAMW || o->momentum != 0.f;
+        const float *w32 = o->master_W ? o->master_W : (a->dtype == LCE_FP32 ? static_cast<const float *>(a->W) : nullptr);
+        if ((use_m && !encode_opt_map(&opt_maps[0], o->exp_avg, true, d, V)) ||
+            (o->kind == LCE_OPT_ADAMW && !encode_opt_map(&opt_maps[1], o->exp_avg_sq, true, d, V)) ||
+            (w32 && !encode_opt_map(&opt_maps[2], w32, true, d, V)) ||
+            (a->dtype == LCE_BF16 && !encode_opt_map(&opt_maps[3], a->W, false, d, V)))
+            return LCE_ERR_CUDA;
         oa.kind = o->kind == LCE_OPT_ADAMW ? OPT_ADAMW : OPT_SGD;
         oa.first = o->step == 1;
         oa.lr = o->lr;
@@ -569,6 +594,10 @@ lce_status_t run_rows(const lce_args_t *a, const DevInfo &di, uint8_t *base, con
             mp.st_g[1] = st_g[g.has_next ? (j + 1) % nbuf : 0][1];
             mp.st_dw = st_dw;
             mp.st_dh = st_dh;
+            mp.opt_m = opt_maps[0];
+            mp.opt_v = opt_maps[1];
+            mp.opt_w32 = opt_maps[2];
+            mp.opt_w16 = opt_maps[3];
             if (j < 0) {
                 bwd_kernel<<<grid, kThreads, kGemmSmem, st>>>(mp, g);
             } else {

@@ -74,6 +74,16 @@ constexpr int kPairTx = 2 * kStageBytes;   // bytes both CTAs land on the even C
 constexpr int kEpiBufBytes = 4096;
 constexpr int kEpiBytes = 4 * 2 * kEpiBufBytes;
 constexpr int kGemmSmem = kStages * kStageBytes + kEpiBytes + 1024 /*alignment slack*/ + 256 /*barriers*/;
+// The optimizer instantiation runs a 5-stage ring: the freed 32 KB doubles
+// each epilogue warp's staging area (16 KB), which holds the ring of W and
+// optimizer-state boxes the TMA engine streams through (the mainloop is as
+// fast with 5 stages as with 6 on these shapes).
+template <int KIND>
+struct Cfg {
+    static constexpr int kS = KIND == 2 /* KIND_BWD_OPT */ ? 5 : kStages;
+    static constexpr int kEpiWarp = (kGemmSmem - kS * kStageBytes - 1024 - 256) / 4;   // staging bytes per warp
+};
+constexpr int kOptLoadBars = 3;   // TMA load barriers per epilogue warp (optimizer ring)
 constexpr long long kWaitCycles = 2000000000LL;   // ~1 s: far above any legitimate wait
 constexpr long long kDrainCycles = 200000000LL;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -142,6 +152,10 @@ struct GemmMaps {
     CUtensorMap st_g[2];
     CUtensorMap st_dw;
     CUtensorMap st_dh;
+    // fused optimizer: {16, 32} boxes of W's state (fp32, 64-byte swizzle:
+    // first moment / momentum buffer, second moment, fp32 weights or master
+    // copy) and of a bf16 W (32-byte swizzle); unused maps stay zero
+    CUtensorMap opt_m, opt_v, opt_w32, opt_w16;
 };
 
 __host__ __device__ constexpr int map_slot(int type) { return type == T_DH ? 1 : (type == T_DW ? 2 : 0); }
@@ -319,87 +333,124 @@ __device__ __forceinline__ void split_bf16(float x, float &hi, float &lo) {
     hi = h;
 }
 
-// Fused optimizer step on elements [off, off + ncol) of W (ncol a multiple of
-// 8, at most 32, zero for none; off a multiple of 8), split in two so that a
-// chunk's global loads are all in flight together (and with the TMEM load of
-// its gradient): opt_load reads the weights and state, opt_apply updates them
-// with gradient g and writes them back.
-struct OptRegs {
-    float w[32], m[32], v[32];
+// Fused optimizer step on one 32-row x 16-column box of W held in a warp's
+// staging buffer, as the TMA engine loaded it: lane r updates row r from its
+// gradient g[0..15] (straight from TMEM). Buffer layout: first moment /
+// momentum buffer (fp32, 2 KB), second moment (fp32, 2 KB), then the weights:
+// fp32 (2 KB; the master copy or an fp32 W) or bf16 (1 KB); with a master
+// copy the bf16 rounding of W follows at 6 KB. fp32 rows of 64 bytes keep
+// 16-byte unit k of row r at unit k ^ ((r >> 1) & 3) (64-byte swizzle), bf16
+// rows of 32 bytes at unit k ^ ((r >> 2) & 1) (32-byte swizzle).
+constexpr int kOptM = 0, kOptV = 2048, kOptW = 4096, kOptWOut = 6144;
+
+__device__ __forceinline__ float4 *opt_f32(uint8_t *buf, int off, int r, int k) {
+    return reinterpret_cast<float4 *>(buf + off + r * 64 + ((k ^ ((r >> 1) & 3)) << 4));
+}
+__device__ __forceinline__ uint4 *opt_b16(uint8_t *buf, int off, int r, int k) {
+    return reinterpret_cast<uint4 *>(buf + off + r * 32 + ((k ^ ((r >> 2) & 1)) << 4));
+}
+
+__device__ __forceinline__ void opt_row(const OptArgs &o, uint8_t *buf, int r, const float *g) {
+    const bool use_m = o.kind == OPT_ADAMW || o.momentum != 0.f;
+    const bool w32 = o.master || o.w_fp32;
+    float w[16], m[16], v[16];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if (w32) {
+            const float4 x = *opt_f32(buf, kOptW, r, k);
+            w[4 * k] = x.x, w[4 * k + 1] = x.y, w[4 * k + 2] = x.z, w[4 * k + 3] = x.w;
+        }
+        if (use_m) {
+            const float4 x = *opt_f32(buf, kOptM, r, k);
+            m[4 * k] = x.x, m[4 * k + 1] = x.y, m[4 * k + 2] = x.z, m[4 * k + 3] = x.w;
+        }
+        if (o.kind == OPT_ADAMW) {
+            const float4 x = *opt_f32(buf, kOptV, r, k);
+            v[4 * k] = x.x, v[4 * k + 1] = x.y, v[4 * k + 2] = x.z, v[4 * k + 3] = x.w;
+        }
+    }
+    if (!w32) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const uint4 x = *opt_b16(buf, kOptW, r, k);
+            const uint32_t u[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                w[8 * k + 2 * i] = __uint_as_float(u[i] << 16);
+                w[8 * k + 2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        if (o.kind == OPT_ADAMW) {
+            w[j] *= 1.f - o.lr * o.wd;
+            m[j] = o.beta1 * m[j] + (1.f - o.beta1) * g[j];
+            v[j] = o.beta2 * v[j] + (1.f - o.beta2) * g[j] * g[j];
+            w[j] -= o.step_size * m[j] / (sqrtf(v[j]) * o.inv_bc2_sqrt + o.eps);
+        } else {
+            float dd = g[j] + o.wd * w[j];
+            if (use_m) {
+                m[j] = o.first ? dd : o.momentum * m[j] + dd;
+                dd = m[j];
+            }
+            w[j] -= o.lr * dd;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if (use_m) *opt_f32(buf, kOptM, r, k) = make_float4(m[4 * k], m[4 * k + 1], m[4 * k + 2], m[4 * k + 3]);
+        if (o.kind == OPT_ADAMW)
+            *opt_f32(buf, kOptV, r, k) = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        if (w32) *opt_f32(buf, kOptW, r, k) = make_float4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+    }
+    if (!o.w_fp32) {
+        const int off = o.master ? kOptWOut : kOptW;
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+            *opt_b16(buf, off, r, k) = make_uint4(pack_bf16x2(w[8 * k], w[8 * k + 1]), pack_bf16x2(w[8 * k + 2], w[8 * k + 3]),
+                                                  pack_bf16x2(w[8 * k + 4], w[8 * k + 5]),
+                                                  pack_bf16x2(w[8 * k + 6], w[8 * k + 7]));
+    }
+}
+
+// One warp's ring of optimizer boxes: `nbuf` buffers of `bsz` bytes, one TMA
+// load barrier each; box p of a dW tile covers W rows [row, row + 32) and
+// columns [col0 + 16p, +16).
+struct OptRing {
+    uint8_t *base;
+    uint64_t *bar;
+    int nbuf, bsz;
+    uint32_t bytes;    // transaction bytes of one box's loads
+    uint32_t phase;    // bit b: parity of buffer b's next completion
+    uint32_t pend;     // bit b: a load into buffer b is in flight
 };
 
-__device__ __forceinline__ void ld8(const float *p, float *x, bool stream) {
-    const float4 a = stream ? __ldcs(reinterpret_cast<const float4 *>(p)) : *reinterpret_cast<const float4 *>(p);
-    const float4 b = stream ? __ldcs(reinterpret_cast<const float4 *>(p) + 1) : *(reinterpret_cast<const float4 *>(p) + 1);
-    x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+// lane 0: load box p (state and weights) into its ring buffer
+__device__ __forceinline__ void opt_issue(const GemmMaps &maps, const OptArgs &o, OptRing &q, int p, int col,
+                                          int row) {
+    const int b = p % q.nbuf;
+    uint8_t *buf = q.base + b * q.bsz;
+    uint64_t *bar = q.bar + b;
+    mbar_arrive_expect_tx(bar, q.bytes);
+    if (o.kind == OPT_ADAMW || o.momentum != 0.f) tma_load_2d(buf + kOptM, &maps.opt_m, bar, col, row);
+    if (o.kind == OPT_ADAMW) tma_load_2d(buf + kOptV, &maps.opt_v, bar, col, row);
+    if (o.master || o.w_fp32)
+        tma_load_2d(buf + kOptW, &maps.opt_w32, bar, col, row);
+    else
+        tma_load_2d(buf + kOptW, &maps.opt_w16, bar, col, row);
+    q.pend |= 1u << b;
 }
 
-__device__ __forceinline__ void st8(float *p, const float *x, bool stream) {
-    const float4 a = make_float4(x[0], x[1], x[2], x[3]), b = make_float4(x[4], x[5], x[6], x[7]);
-    if (stream) {
-        __stcs(reinterpret_cast<float4 *>(p), a);
-        __stcs(reinterpret_cast<float4 *>(p) + 1, b);
-    } else {
-        *reinterpret_cast<float4 *>(p) = a;
-        *(reinterpret_cast<float4 *>(p) + 1) = b;
-    }
-}
-
-__device__ __forceinline__ void opt_load(const OptArgs &o, size_t off, int ncol, OptRegs &s) {
-    const bool use_m = o.kind == OPT_ADAMW || o.momentum != 0.f;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        if (q * 8 < ncol) {
-            const size_t e = off + q * 8;
-            if (o.master || o.w_fp32) {
-                ld8((o.master ? o.master : static_cast<const float *>(o.W)) + e, s.w + q * 8, false);
-            } else {
-                const uint4 x = *reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(o.W) + e);
-                const uint32_t u[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    s.w[q * 8 + 2 * k] = __uint_as_float(u[k] << 16);
-                    s.w[q * 8 + 2 * k + 1] = __uint_as_float(u[k] & 0xffff0000u);
-                }
-            }
-            if (use_m) ld8(o.m + e, s.m + q * 8, true);
-            if (o.kind == OPT_ADAMW) ld8(o.v + e, s.v + q * 8, true);
-        }
-    }
-}
-
-__device__ __forceinline__ void opt_apply(const OptArgs &o, size_t off, int ncol, OptRegs &s, const float (&g)[32]) {
-    const bool use_m = o.kind == OPT_ADAMW || o.momentum != 0.f;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        if (o.kind == OPT_ADAMW) {
-            s.w[j] *= 1.f - o.lr * o.wd;
-            s.m[j] = o.beta1 * s.m[j] + (1.f - o.beta1) * g[j];
-            s.v[j] = o.beta2 * s.v[j] + (1.f - o.beta2) * g[j] * g[j];
-            s.w[j] -= o.step_size * s.m[j] / (sqrtf(s.v[j]) * o.inv_bc2_sqrt + o.eps);
-        } else {
-            float d = g[j] + o.wd * s.w[j];
-            if (use_m) {
-                s.m[j] = o.first ? d : o.momentum * s.m[j] + d;
-                d = s.m[j];
-            }
-            s.w[j] -= o.lr * d;
-        }
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        if (q * 8 < ncol) {
-            const size_t e = off + q * 8;
-            const float *w = s.w + q * 8;
-            if (use_m) st8(o.m + e, s.m + q * 8, true);
-            if (o.kind == OPT_ADAMW) st8(o.v + e, s.v + q * 8, true);
-            if (o.master || o.w_fp32) st8((o.master ? o.master : static_cast<float *>(o.W)) + e, w, false);
-            if (!o.w_fp32)
-                *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(o.W) + e) =
-                    make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]), pack_bf16x2(w[4], w[5]),
-                               pack_bf16x2(w[6], w[7]));
-        }
-    }
+// lane 0: store box p back (rows past V and columns past d are clipped)
+__device__ __forceinline__ void opt_store(const GemmMaps &maps, const OptArgs &o, const OptRing &q, int p, int col,
+                                          int row) {
+    const uint8_t *buf = q.base + (p % q.nbuf) * q.bsz;
+    if (o.kind == OPT_ADAMW || o.momentum != 0.f) tma_store_2d(&maps.opt_m, buf + kOptM, col, row);
+    if (o.kind == OPT_ADAMW) tma_store_2d(&maps.opt_v, buf + kOptV, col, row);
+    if (o.master || o.w_fp32) tma_store_2d(&maps.opt_w32, buf + kOptW, col, row);
+    if (!o.w_fp32) tma_store_2d(&maps.opt_w16, buf + (o.master ? kOptWOut : kOptW), col, row);
+    bulk_commit_group();
 }
 
 // Issue this CTA's TMA loads of one k-block (A rows am.., B rows bn.., k0..)
@@ -447,6 +498,7 @@ template <int KIND, bool kGather>
 __device__ __forceinline__ void producer(const GemmMaps &maps, const GemmArgs &a, const Sched &s, int pair,
                                          int npairs, uint32_t rank, int lane, uint8_t *smem, uint64_t *full,
                                          uint64_t *empty, uint32_t full_even, volatile int *abort_flag) {
+    constexpr int S = Cfg<KIND>::kS;
     int it = 0;
     bool ok = true;
     bool dep_done = false;
@@ -476,7 +528,7 @@ __device__ __forceinline__ void producer(const GemmMaps &maps, const GemmArgs &a
             int4 rows_next = rows;
             if (gB && k_blocks > 0) rows_next = idx4[(lane & 15)];
             for (int kbt = 0; kbt < k_blocks; ++kbt, ++it) {
-                const int st = it % kStages;
+                const int st = it % S;
                 if (gB) {
                     // token rows of this k-block; the next block's are fetched
                     // before the wait so that their latency overlaps it
@@ -485,12 +537,12 @@ __device__ __forceinline__ void producer(const GemmMaps &maps, const GemmArgs &a
                 }
                 if (kGather) {
                     bool got = true;
-                    if (lane == 0) got = wait_bar(&empty[st], ((it / kStages) & 1) ^ 1, abort_flag);
+                    if (lane == 0) got = wait_bar(&empty[st], ((it / S) & 1) ^ 1, abort_flag);
                     if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
                         ok = false;
                         break;
                     }
-                } else if (!wait_bar(&empty[st], ((it / kStages) & 1) ^ 1, abort_flag)) {
+                } else if (!wait_bar(&empty[st], ((it / S) & 1) ^ 1, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -524,8 +576,8 @@ __device__ __forceinline__ void producer(const GemmMaps &maps, const GemmArgs &a
     }
     if (!ok && rank == 0 && lane == 0) {
         // let the copies already issued (by both CTAs) land before the pair exits
-        const int first = it > kStages ? it - kStages : 0;
-        for (int j = first; j < it; ++j) drain_bar(&full[j % kStages], (j / kStages) & 1);
+        const int first = it > S ? it - S : 0;
+        for (int j = first; j < it; ++j) drain_bar(&full[j % S], (j / S) & 1);
     }
 }
 
@@ -542,15 +594,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     constexpr uint32_t kIdescKM = idesc_f32acc(kFmtBf16, kPairM, kBN, false, true);    // DH
     constexpr uint32_t kIdescMM = idesc_f32acc(kFmtBf16, kPairM, kBN, true, true);     // DW
 
+    constexpr int S = Cfg<KIND>::kS;          // pipeline stages
+    constexpr int EW = Cfg<KIND>::kEpiWarp;   // staging bytes per epilogue warp
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *epi_stage = smem + kStages * kStageBytes;                            // epilogue staging buffers
-    uint64_t *full = reinterpret_cast<uint64_t *>(epi_stage + kEpiBytes);          // used on the even CTA
-    uint64_t *empty = full + kStages;
-    uint64_t *tfull = empty + kStages;
+    uint8_t *epi_stage = smem + S * kStageBytes;                                  // epilogue staging buffers
+    uint64_t *full = reinterpret_cast<uint64_t *>(epi_stage + 4 * EW);             // used on the even CTA
+    uint64_t *empty = full + S;
+    uint64_t *tfull = empty + S;
     uint64_t *tempty = tfull + 2;                                                   // used on the even CTA
     uint64_t *mma_done = tempty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    uint64_t *opt_bar = mma_done + 1;                                               // optimizer ring (4 x 3)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(opt_bar + 4 * kOptLoadBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -563,10 +618,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (pair >= s.units) return;   // uniform over both CTAs of the pair
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
+        if (KIND == KIND_BWD_OPT)
+            for (int i = 0; i < 4 * kOptLoadBars; ++i) mbar_init(&opt_bar[i], 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
             mbar_init(&tempty[i], 8);   // 4 epilogue warps in each CTA of the pair
@@ -624,8 +681,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + acc * kBN;
                     for (int kb = 0; kb < k_blocks; ++kb, ++it) {
-                        const int st = it % kStages;
-                        if (!wait_bar(&full[st], (it / kStages) & 1, abort_flag)) {
+                        const int st = it % S;
+                        if (!wait_bar(&full[st], (it / S) & 1, abort_flag)) {
                             ok = false;
                             break;
                         }
@@ -653,7 +710,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ epilogue
         const int quarter = warp & 3;
         const int trow = quarter * 32 + lane;     // row within this CTA's 128 rows == TMEM lane
-        uint8_t *stage_mine = epi_stage + (warp - 2) * 2 * kEpiBufBytes;   // this warp's two staging buffers
+        uint8_t *stage_mine = epi_stage + (warp - 2) * EW;   // this warp's staging buffers
+        // fused optimizer: this warp's ring of W / state boxes in its staging
+        // area (three 5 KB buffers, or two 8 KB ones when fp32 weights move)
+        OptRing ring{};
+        if (KIND == KIND_BWD_OPT) {
+            const bool w32 = a.opt.master || a.opt.w_fp32;
+            ring.base = stage_mine;
+            ring.bar = opt_bar + (warp - 2) * kOptLoadBars;
+            ring.nbuf = w32 ? 2 : 3;
+            ring.bsz = w32 ? 8192 : 5120;
+            ring.bytes = ((a.opt.kind == OPT_ADAMW || a.opt.momentum != 0.f) ? 2048u : 0u) +
+                         (a.opt.kind == OPT_ADAMW ? 2048u : 0u) + (w32 ? 2048u : 1024u);
+        }
         int ebuf = 0;
         const float gscale = a.grad_ptr ? a.grad_scale * *a.grad_ptr : a.grad_scale;
         const int nvn = *a.nv_norm;
@@ -684,21 +753,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     lse2 = a.lse2[grow];
                 }
                 const int acc = tile & 1;
+                const bool opt_dw = KIND == KIND_BWD_OPT && t.type == T_DW;
+                // fused optimizer: this warp's 32 W rows and the tile's 16-column boxes
+                // that lie inside d; the first boxes' loads do not depend on the
+                // accumulator and are issued before waiting for it
+                const int opt_row0 = a.v0w + t.mb * kPairM + static_cast<int>(rank) * kBM + quarter * 32;
+                const int opt_col0 = t.nt * kBN;
+                const int opt_np = opt_dw ? (a.d - opt_col0 >= kBN ? kBN / 16 : cdiv(a.d - opt_col0, 16)) : 0;
+                if (opt_dw) {
+                    if (lane == 0) {
+                        bulk_wait_group_read<0>();   // earlier stores have read the staging area
+                        for (int p = 0; p < ring.nbuf && p < opt_np; ++p)
+                            opt_issue(maps, a.opt, ring, p, opt_col0 + 16 * p, opt_row0);
+                    }
+                    __syncwarp();
+                }
                 if (!wait_bar(&tfull[acc], (tile >> 1) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kBN;
-                const bool opt_dw = KIND == KIND_BWD_OPT && t.type == T_DW;
 #pragma unroll 1
                 for (int c = 0; c < kBN / 32; ++c) {
                     const int col = t.nt * kBN + c * 32;   // column within the vocab range / d
-                    // fused optimizer: this thread's W row slice [off, off + ncol)
-                    const size_t opt_off = static_cast<size_t>(a.v0w + grow) * a.d + col;
-                    const int opt_ncol = (opt_dw && grow < a.vlenw && col < a.d) ? (a.d - col < 32 ? a.d - col : 32) : 0;
-                    OptRegs ost;
-                    if (opt_ncol) opt_load(a.opt, opt_off, opt_ncol, ost);
+                    if (opt_dw && 2 * c >= opt_np) break;   // boxes past d: nothing to update
                     uint32_t r[32];
                     tmem_ld32(tbase + c * 32, r);
                     tmem_ld_wait();
@@ -743,8 +822,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             for (int j = 0; j < 32; ++j) v[j] = zero_acc ? 0.f : __uint_as_float(r[j]);
                         }
                         if (opt_dw) {
-                            // fused optimizer: update the W row slice in place, no dW store
-                            if (opt_ncol) opt_apply(a.opt, opt_off, opt_ncol, ost, v);
+                            // fused optimizer: boxes 2c and 2c+1 (16 columns each) of the
+                            // ring; lane = W row; no dW store
+                            bool box_ok = true;
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const int p = 2 * c + h;
+                                if (p >= opt_np) break;
+                                const int b = p % ring.nbuf;
+                                if (!wait_bar(ring.bar + b, (ring.phase >> b) & 1u, abort_flag)) {
+                                    box_ok = false;
+                                    break;
+                                }
+                                ring.phase ^= 1u << b;
+                                ring.pend &= ~(1u << b);
+                                opt_row(a.opt, ring.base + b * ring.bsz, lane, v + 16 * h);
+                                fence_proxy_async_smem();
+                                __syncwarp();
+                                if (lane == 0) {
+                                    opt_store(maps, a.opt, ring, p, opt_col0 + 16 * p, opt_row0);
+                                    if (p + ring.nbuf < opt_np) {
+                                        bulk_wait_group_read<0>();   // the store has read the buffer
+                                        opt_issue(maps, a.opt, ring, p + ring.nbuf, opt_col0 + 16 * (p + ring.nbuf),
+                                                  opt_row0);
+                                    }
+                                }
+                                __syncwarp();
+                            }
+                            if (!box_ok) {
+                                ok = false;
+                                break;
+                            }
                             continue;
                         }
                         uint8_t *sbuf = stage_mine + ebuf * kEpiBufBytes;
@@ -803,11 +911,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(tempty_even + acc * 8);
+                if (opt_dw) {
+                    // the ring overlaps the staging buffers the next tiles write
+                    if (lane == 0) bulk_wait_group_read<0>();
+                    __syncwarp();
+                }
             }
             if (KIND == KIND_LSE && ok && grow < nv) {
                 const int split = u / s.m_blocks;
                 a.part[static_cast<size_t>(split) * s.m_blocks * kPairM + grow] = make_float2(run_m, run_l);
             }
+        }
+        if (KIND == KIND_BWD_OPT && lane == 0) {
+            // after an abort: let optimizer loads still in flight land first
+            for (int b = 0; b < ring.nbuf; ++b)
+                if (ring.pend & (1u << b)) drain_bar(ring.bar + b, (ring.phase >> b) & 1u);
         }
         if (lane == 0) bulk_wait_group_all();   // this warp's stores have written global memory
     }
