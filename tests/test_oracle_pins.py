@@ -341,3 +341,52 @@ def test_zero_gradient_without_decay_only_decays_the_moments():
     np.testing.assert_allclose(r["exp_avg_sq"], 0.99 * v)
     s = oracle.optimizer_step("sgd", w, g0, lr=0.1, step=3)
     np.testing.assert_array_equal(s["w"], w)
+
+
+# ------------------------------------ input-embedding lookup skipping padding
+
+def _emb_case(seed=3, N=57, d=6, V=13, pad=0):
+    g = np.random.default_rng(seed)
+    W = g.standard_normal((V, d))
+    t = g.integers(0, V, N)
+    t[g.random(N) < 0.3] = pad
+    dE = g.standard_normal((N, d))
+    return W, t, dE
+
+
+def test_embedding_matches_torch_autograd_of_masked_lookup():
+    torch = pytest.importorskip("torch")
+    W, t, dE = _emb_case()
+    pad = 0
+    Wt = torch.tensor(W, requires_grad=True)
+    mask = torch.tensor(t != pad, dtype=torch.float64)[:, None]
+    E = torch.nn.functional.embedding(torch.tensor(t), Wt) * mask
+    (E * torch.tensor(dE)).sum().backward()
+    np.testing.assert_allclose(oracle.embedding_forward(W, t, pad), E.detach().numpy(), rtol=0, atol=0)
+    np.testing.assert_allclose(oracle.embedding_backward(dE, t, pad, W.shape[0]), Wt.grad.numpy(),
+                               rtol=1e-14, atol=1e-14)
+
+
+def test_embedding_invariants():
+    W, t, dE = _emb_case(seed=5, pad=2)
+    pad, V = 2, W.shape[0]
+    valid = t != pad
+    E = oracle.embedding_forward(W, t, pad)
+    assert np.all(E[~valid] == 0.0) and np.array_equal(E[valid], W[t[valid]])
+    dW = oracle.embedding_backward(dE, t, pad, V)
+    np.testing.assert_allclose(dW.sum(0), dE[valid].sum(0), rtol=1e-12, atol=1e-12)
+    untouched = np.setdiff1d(np.arange(V), t[valid])
+    assert np.all(dW[untouched] == 0.0)
+    assert np.all(dW[pad] == 0.0)          # the padding id never receives a gradient
+    perm = np.random.default_rng(0).permutation(len(t))
+    np.testing.assert_allclose(oracle.embedding_backward(dE[perm], t[perm], pad, V), dW, rtol=1e-13, atol=1e-13)
+
+
+def test_embedding_refuses_out_of_range_tokens():
+    W, t, dE = _emb_case()
+    t = t.copy()
+    t[4] = W.shape[0]
+    with pytest.raises(ValueError):
+        oracle.embedding_forward(W, t, 0)
+    with pytest.raises(ValueError):
+        oracle.embedding_backward(dE, t, 0, W.shape[0])
