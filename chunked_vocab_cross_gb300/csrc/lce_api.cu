@@ -30,6 +30,7 @@
 #include <vector>
 
 #include "lce.h"
+#include "lce_embed.cuh"
 #include "lce_gemm.cuh"
 #include "lce_rows.cuh"
 
@@ -808,6 +809,120 @@ lce_status_t lce_compact(const int64_t *targets, int64_t N, int64_t ignore_index
     PhaseScope ph(0, st);
     k_compact<<<1, kCompactThreads, 0, st>>>(targets, static_cast<int>(N), ignore_index, V, idx, inv, counts,
                                              nullptr);
+    LCE_CHECK_LAUNCH();
+    return LCE_OK;
+}
+
+// ------------------------------------------------- input-embedding lookup
+
+namespace {
+struct EmbLayout {
+    size_t kA, vA, kB, vB, seg, counts, finals, total;
+};
+EmbLayout emb_layout(int64_t N) {
+    EmbLayout L{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o += up256(bytes);
+        return at;
+    };
+    L.kA = take(N * 4);
+    L.vA = take(N * 4);
+    L.kB = take(N * 4);
+    L.vB = take(N * 4);
+    L.seg = take((N + 1) * 4);
+    L.counts = take(16);
+    L.finals = take(2 * sizeof(int *));
+    L.total = o;
+    return L;
+}
+
+lce_status_t check_emb(lce_dtype_t dtype, const void *a, const void *b, const int64_t *tokens, int64_t N, int64_t d,
+                       int64_t V) {
+    if (dtype != LCE_BF16 && dtype != LCE_FP32) return LCE_ERR_DTYPE;
+    if (!a || !b || !tokens) return LCE_ERR_NULL;
+    if (N < 1 || N >= (int64_t(1) << 31) || d < 1 || d > 65536 || V < 1 || V >= (int64_t(1) << 31))
+        return LCE_ERR_SHAPE;
+    if (d % 8 || (reinterpret_cast<uintptr_t>(a) & 15u) || (reinterpret_cast<uintptr_t>(b) & 15u))
+        return LCE_ERR_ALIGN;
+    return LCE_OK;
+}
+}  // namespace
+
+lce_status_t lce_embedding_forward(lce_dtype_t dtype, const void *W, const int64_t *tokens, int64_t pad_id, int64_t N,
+                                   int64_t d, int64_t V, void *E, lce_stream_t stream) {
+    lce_status_t s = check_emb(dtype, W, E, tokens, N, d, V);
+    if (s != LCE_OK) return s;
+    DevInfo *di = nullptr;
+    s = device_info(&di);
+    if (s != LCE_OK) return s;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int rows_per_block = 256 / 32;
+    const int64_t want = (N + rows_per_block - 1) / rows_per_block;
+    const int grid = static_cast<int>(want < 8 * di->sms ? want : 8 * di->sms);
+    if (dtype == LCE_BF16)
+        k_emb_forward<__nv_bfloat16><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(W), tokens, pad_id,
+                                                            static_cast<int>(N), static_cast<int>(d), V,
+                                                            static_cast<__nv_bfloat16 *>(E));
+    else
+        k_emb_forward<float><<<grid, 256, 0, st>>>(static_cast<const float *>(W), tokens, pad_id, static_cast<int>(N),
+                                                   static_cast<int>(d), V, static_cast<float *>(E));
+    LCE_CHECK_LAUNCH();
+    return LCE_OK;
+}
+
+size_t lce_embedding_workspace_size(int64_t N) {
+    if (N < 1 || N >= (int64_t(1) << 31)) return 0;
+    return emb_layout(N).total;
+}
+
+lce_status_t lce_embedding_backward(lce_dtype_t dtype, const void *dE, const int64_t *tokens, int64_t pad_id,
+                                    int64_t N, int64_t d, int64_t V, float *dW, int accumulate, void *workspace,
+                                    size_t workspace_bytes, lce_stream_t stream) {
+    lce_status_t s = check_emb(dtype, dE, dW, tokens, N, d, V);
+    if (s != LCE_OK) return s;
+    const EmbLayout L = emb_layout(N);
+    if (workspace && (workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 15u)))
+        return workspace_bytes < L.total ? LCE_ERR_WORKSPACE : LCE_ERR_ALIGN;
+    DevInfo *di = nullptr;
+    s = device_info(&di);
+    if (s != LCE_OK) return s;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    WsGuard ws;
+    ws.s = st;
+    if (workspace) {
+        ws.p = workspace;
+    } else {
+        cudaError_t e = cudaMallocAsync(&ws.p, L.total, st);
+        if (e != cudaSuccess) {
+            t_last_cuda = e;
+            return LCE_ERR_CUDA;
+        }
+        ws.owned = true;
+    }
+    uint8_t *base = static_cast<uint8_t *>(ws.p);
+    auto ip = [&](size_t off) { return reinterpret_cast<int *>(base + off); };
+    int **finals = reinterpret_cast<int **>(base + L.finals);
+    if (!accumulate) {
+        const size_t n = static_cast<size_t>(V) * d;
+        k_zero_f32<<<4 * di->sms, 256, 0, st>>>(dW, n);
+        LCE_CHECK_LAUNCH();
+    }
+    k_emb_sort<<<1, kEmbSortThreads, 0, st>>>(tokens, static_cast<int>(N), pad_id, V, ip(L.kA), ip(L.vA), ip(L.kB),
+                                               ip(L.vB), ip(L.seg), ip(L.counts), finals, finals + 1);
+    LCE_CHECK_LAUNCH();
+    const int64_t segs_max = N;
+    dim3 grid(static_cast<unsigned>(segs_max < 4 * di->sms ? segs_max : 4 * di->sms),
+              static_cast<unsigned>((d + kEmbSegCols - 1) / kEmbSegCols));
+    if (dtype == LCE_BF16)
+        k_emb_segsum<__nv_bfloat16><<<grid, kEmbSegCols / 4, 0, st>>>(
+            static_cast<const __nv_bfloat16 *>(dE), finals, finals + 1, ip(L.seg), ip(L.counts), static_cast<int>(d),
+            dW, accumulate ? 1 : 0);
+    else
+        k_emb_segsum<float><<<grid, kEmbSegCols / 4, 0, st>>>(static_cast<const float *>(dE), finals, finals + 1,
+                                                              ip(L.seg), ip(L.counts), static_cast<int>(d), dW,
+                                                              accumulate ? 1 : 0);
     LCE_CHECK_LAUNCH();
     return LCE_OK;
 }

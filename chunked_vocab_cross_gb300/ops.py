@@ -299,3 +299,60 @@ class FusedOptimizer:
             self.step_count -= 1
             raise
         return loss, dH
+
+
+def embedding_forward(W, tokens, pad_id: int = 0, *, stream=None):
+    """E [N, d] (W's dtype): rows of W for the tokens, zero rows where the token
+    is pad_id; non-padding ids outside [0, V) give zero rows and set the
+    target-range bit of the device status word."""
+    if not (W.is_cuda and tokens.is_cuda) or W.dtype not in _DT or tokens.dtype != torch.int64:
+        raise ValueError("W must be a bf16/fp32 CUDA tensor and tokens int64 on the same device")
+    if W.dim() != 2 or tokens.dim() != 1 or not W.is_contiguous():
+        raise ValueError("W must be a contiguous [V, d] tensor and tokens [N]")
+    tokens = tokens.contiguous()
+    E = torch.empty((tokens.shape[0], W.shape[1]), dtype=W.dtype, device=W.device)
+    _abi.check(_abi.lib().lce_embedding_forward(_DT[W.dtype], W.data_ptr(), tokens.data_ptr(), int(pad_id),
+                                                tokens.shape[0], W.shape[1], W.shape[0], E.data_ptr(),
+                                                _stream(stream)), "lce_embedding_forward")
+    return E
+
+
+def embedding_backward(dE, tokens, pad_id: int, V: int, *, dW=None, accumulate: bool = False, stream=None):
+    """dW [V, d] fp32 with each token's gradient rows summed in ascending
+    position order (overwritten, or added into a given dW with accumulate)."""
+    if not (dE.is_cuda and tokens.is_cuda) or dE.dtype not in _DT or tokens.dtype != torch.int64:
+        raise ValueError("dE must be a bf16/fp32 CUDA tensor and tokens int64 on the same device")
+    if dE.dim() != 2 or tokens.dim() != 1 or dE.shape[0] != tokens.shape[0]:
+        raise ValueError("dE must be [N, d] and tokens [N]")
+    dE, tokens = dE.contiguous(), tokens.contiguous()
+    if dW is None:
+        dW = torch.empty((V, dE.shape[1]), dtype=torch.float32, device=dE.device)
+        accumulate = False
+    elif dW.dtype != torch.float32 or dW.shape != (V, dE.shape[1]) or not dW.is_contiguous():
+        raise ValueError("dW must be a contiguous fp32 [V, d] tensor")
+    _abi.check(_abi.lib().lce_embedding_backward(_DT[dE.dtype], dE.data_ptr(), tokens.data_ptr(), int(pad_id),
+                                                 tokens.shape[0], dE.shape[1], V, dW.data_ptr(),
+                                                 1 if accumulate else 0, None, 0, _stream(stream)),
+               "lce_embedding_backward")
+    return dW
+
+
+class _Embedding(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, W, tokens, pad_id):
+        ctx.save_for_backward(tokens)
+        ctx.pad_id, ctx.V, ctx.w_dtype = pad_id, W.shape[0], W.dtype
+        return embedding_forward(W, tokens, pad_id)
+
+    @staticmethod
+    def backward(ctx, dE):
+        (tokens,) = ctx.saved_tensors
+        dW = embedding_backward(dE.to(ctx.w_dtype).contiguous(), tokens, ctx.pad_id, ctx.V)
+        return dW.to(ctx.w_dtype), None, None
+
+
+def embedding(W, tokens, pad_id: int = 0):
+    """Autograd input-embedding lookup that skips padding (zero rows, no
+    gradient); with a W tied to the output projection its gradient adds to
+    linear_cross_entropy's through autograd."""
+    return _Embedding.apply(W, tokens, pad_id)

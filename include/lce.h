@@ -280,6 +280,40 @@ lce_status_t lce_forward_noalloc(const void *H, const void *W, const int64_t *ta
  */
 lce_status_t lce_selftest_wait_timeout(int64_t cycles, int32_t *gave_up, lce_stream_t stream);
 
+/*
+ * Input-embedding lookup that skips padding, for a vocabulary matrix W shared
+ * by the input lookup and the output projection ("6GB显卡预训练11亿参数模型",
+ * section "关键参数说明", --tie-embeddings):
+ *   E[i,:] = W[tokens[i],:] where tokens[i] != pad_id, a zero row where it is.
+ * The valid mask and the lookup run in one kernel with no host
+ * synchronisation ("为什么26万词表会卡死16GB显卡", section 2.3 稀疏索引引擎).
+ * W [V,d] and E [N,d] are device arrays of `dtype`; tokens [N] int64.
+ * A non-padding token outside [0, V) gets a zero row and sets
+ * LCE_DEV_TARGET_RANGE in the device status word. Same shape, alignment and
+ * error rules as lce_run (d % 8 == 0, 16-byte aligned W and E).
+ */
+lce_status_t lce_embedding_forward(lce_dtype_t dtype, const void *W, const int64_t *tokens, int64_t pad_id,
+                                   int64_t N, int64_t d, int64_t V, void *E, lce_stream_t stream);
+
+/*
+ * Gradient of lce_embedding_forward with respect to W:
+ *   dW[v,:] (+)= sum of dE[i,:] over the positions i with tokens[i] == v,
+ * for tokens that are not pad_id and lie in [0, V) (others are skipped and
+ * flagged as in the forward). dE [N,d] of `dtype`, dW [V,d] fp32 (device).
+ * accumulate = 0 overwrites dW (rows of tokens that do not occur become 0);
+ * nonzero adds into it, so for a tied W the output projection's dW (lce_run)
+ * and this gradient sum into one buffer. Each row's sum is taken in ascending
+ * position order after the positions are grouped by token on the device (the
+ * batch's per-token gradients aggregated after backward, same page, section
+ * 2.2, without atomics): results are reproducible bit for bit.
+ * Scratch: lce_embedding_workspace_size(N) bytes of `workspace` (device,
+ * 16-byte aligned), or NULL for a stream-ordered allocation.
+ */
+size_t lce_embedding_workspace_size(int64_t N);
+lce_status_t lce_embedding_backward(lce_dtype_t dtype, const void *dE, const int64_t *tokens, int64_t pad_id,
+                                    int64_t N, int64_t d, int64_t V, float *dW, int accumulate, void *workspace,
+                                    size_t workspace_bytes, lce_stream_t stream);
+
 /* ABI version: major*10000 + minor*100 + patch. */
 int lce_version(void);
 

@@ -163,3 +163,19 @@ def test_row_gather_option_checks_without_gpu(lib):
     full = lib.lce_workspace_size_args(ctypes.byref(b))
     b.row_gather = 1
     assert full - lib.lce_workspace_size_args(ctypes.byref(b)) == 1024 * 512 * 2
+
+
+def test_embedding_entry_points_host_checks_without_gpu(lib):
+    f, b = lib.lce_embedding_forward, lib.lce_embedding_backward
+    assert f(0, None, 4096, 0, 10, 64, 100, 4096, None) == 1             # NULL W
+    assert f(0, 4096, 4096, 0, 0, 64, 100, 4096, None) == 2              # N < 1
+    assert f(0, 4096, 4096, 0, 10, 12, 100, 4096, None) == 3             # d % 8
+    assert f(0, 4100, 4096, 0, 10, 64, 100, 4096, None) == 3             # misaligned W
+    assert f(7, 4096, 4096, 0, 10, 64, 100, 4096, None) == 4             # dtype
+    assert b(0, 4096, 4096, 0, 10, 64, 0, 4096, 0, None, 0, None) == 2   # V < 1
+    assert b(0, 4096, None, 0, 10, 64, 100, 4096, 0, None, 0, None) == 1
+    ws = lib.lce_embedding_workspace_size(10)
+    assert ws > 0 and lib.lce_embedding_workspace_size(0) == 0
+    assert b(0, 4096, 4096, 0, 10, 64, 100, 4096, 0, 8192, ws - 1, None) == 6   # workspace too small
+    # scratch grows with N only (grouping the positions), never with V or d
+    assert lib.lce_embedding_workspace_size(16384) < 16384 * 32
