@@ -197,6 +197,64 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_embedding(args):
+    """Input-embedding lookup skipping padding + its gradient accumulated into
+    an fp32 dW (the tied-W training step's input side), on the workload's
+    tokens (padding -> id 0). HBM-bound: the roofline is algorithmic bytes
+    (valid W rows read, E written, valid dE rows read, the touched dW rows
+    read and written) over the measured copy bandwidth."""
+    import torch
+
+    import chunked_vocab_cross_gb300 as lce
+    from chunked_vocab_cross_gb300.build import build
+    from synth_inputs import make_inputs
+    torch.cuda.set_device(0)
+    build()
+    x = make_inputs(args.workload)
+    w = x.workload
+    pad = 0
+    tok = np.where(x.targets == -100, pad, x.targets)
+    nv = int((tok != pad).sum())
+    distinct = int(np.unique(tok[tok != pad]).size)
+    W = torch.from_numpy(x.W.view(np.int16)).view(torch.bfloat16).cuda()
+    t = torch.from_numpy(tok).cuda()
+    dE = torch.randn(w.N, w.d, device="cuda").to(torch.bfloat16)
+    dW = torch.zeros(w.V, w.d, dtype=torch.float32, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")   # 256 MB > L2, written between steps
+
+    def step():
+        lce.embedding_forward(W, t, pad)
+        lce.embedding_backward(dE, t, pad, w.V, dW=dW, accumulate=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        step()
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    status = lce.device_status()
+    med = float(np.median(ms))
+    bytes_alg = nv * w.d * 2 + w.N * w.d * 2 + nv * w.d * 2 + distinct * w.d * 8
+    peaks, src = load_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    gbs = bytes_alg / (med / 1e3) / 1e9
+    print(json.dumps({
+        "metric": "input-embedding lookup + gradient (tied W), tokens/s", "value": w.N / (med / 1e3),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": med,
+        "higher_is_better": True, "dtype": "bf16 (fp32 dW)", "data": "synthetic",
+        "config": {"workload": w.name, "N": w.N, "d": w.d, "V": w.V, "valid": nv, "distinct_tokens": distinct,
+                   "l2": "256 MB buffer written between steps"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "traffic": None, "peak_kind": f"hbm_gbs ({src})", "bytes_per_step": bytes_alg},
+        "device_status": status}), flush=True)
+
+
 def eager_context(H, W, t, nv, steps):
     """Context only (not a baseline of this metric's reference arm): the same
     fwd+bwd in eager PyTorch, which materialises the N x V logits (cuBLAS bf16
@@ -258,6 +316,8 @@ def main():
                     help="forward (storing the per-row lse) and backward from the stored lse as two calls")
     ap.add_argument("--token-chunk", type=int, default=0,
                     help="process the rows this many positions at a time (0 = all at once)")
+    ap.add_argument("--embedding", action="store_true",
+                    help="time the input-embedding lookup + its gradient (tied W) instead of the loss path")
     ap.add_argument("--no-context", action="store_true",
                     help="skip the eager PyTorch context measurement (logits materialised)")
     ap.add_argument("--row-gather", action="store_true",
@@ -265,6 +325,9 @@ def main():
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.embedding:
+        run_embedding(args)
         return
 
     import torch

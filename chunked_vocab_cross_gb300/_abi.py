@@ -46,7 +46,7 @@ SIGNATURES = {
     "lce_selftest_wait_timeout": (c_int, [c_int64, c_void_p, c_void_p]),
     "lce_embedding_forward": (c_int, [c_int, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int64, c_void_p,
                                       c_void_p]),
-    "lce_embedding_workspace_size": (c_size_t, [c_int64]),
+    "lce_embedding_workspace_size": (c_size_t, [c_int64, c_int64]),
     "lce_embedding_backward": (c_int, [c_int, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int64, c_void_p, c_int,
                                        c_void_p, c_size_t, c_void_p]),
 }

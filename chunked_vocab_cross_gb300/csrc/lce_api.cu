@@ -817,9 +817,9 @@ lce_status_t lce_compact(const int64_t *targets, int64_t N, int64_t ignore_index
 
 namespace {
 struct EmbLayout {
-    size_t kA, vA, kB, vB, seg, counts, finals, total;
+    size_t kA, vA, kB, vB, seg, pstart, pseg, pslot, mseg, mslot, mnp, counts, finals, partial, total;
 };
-EmbLayout emb_layout(int64_t N) {
+EmbLayout emb_layout(int64_t N, int64_t d) {
     EmbLayout L{};
     size_t o = 0;
     auto take = [&](size_t bytes) {
@@ -827,13 +827,21 @@ EmbLayout emb_layout(int64_t N) {
         o += up256(bytes);
         return at;
     };
+    const size_t pmax = static_cast<size_t>(emb_pieces_max(N));
     L.kA = take(N * 4);
     L.vA = take(N * 4);
     L.kB = take(N * 4);
     L.vB = take(N * 4);
     L.seg = take((N + 1) * 4);
+    L.pstart = take(pmax * 4);
+    L.pseg = take(pmax * 4);
+    L.pslot = take(pmax * 4);
+    L.mseg = take(N * 4);
+    L.mslot = take(N * 4);
+    L.mnp = take(N * 4);
     L.counts = take(16);
     L.finals = take(2 * sizeof(int *));
+    L.partial = take(static_cast<size_t>(emb_slots_max(N)) * d * 4);
     L.total = o;
     return L;
 }
@@ -872,9 +880,9 @@ lce_status_t lce_embedding_forward(lce_dtype_t dtype, const void *W, const int64
     return LCE_OK;
 }
 
-size_t lce_embedding_workspace_size(int64_t N) {
-    if (N < 1 || N >= (int64_t(1) << 31)) return 0;
-    return emb_layout(N).total;
+size_t lce_embedding_workspace_size(int64_t N, int64_t d) {
+    if (N < 1 || N >= (int64_t(1) << 31) || d < 1 || d > 65536) return 0;
+    return emb_layout(N, d).total;
 }
 
 lce_status_t lce_embedding_backward(lce_dtype_t dtype, const void *dE, const int64_t *tokens, int64_t pad_id,
@@ -882,7 +890,7 @@ lce_status_t lce_embedding_backward(lce_dtype_t dtype, const void *dE, const int
                                     size_t workspace_bytes, lce_stream_t stream) {
     lce_status_t s = check_emb(dtype, dE, dW, tokens, N, d, V);
     if (s != LCE_OK) return s;
-    const EmbLayout L = emb_layout(N);
+    const EmbLayout L = emb_layout(N, d);
     if (workspace && (workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 15u)))
         return workspace_bytes < L.total ? LCE_ERR_WORKSPACE : LCE_ERR_ALIGN;
     DevInfo *di = nullptr;
@@ -903,26 +911,40 @@ lce_status_t lce_embedding_backward(lce_dtype_t dtype, const void *dE, const int
     }
     uint8_t *base = static_cast<uint8_t *>(ws.p);
     auto ip = [&](size_t off) { return reinterpret_cast<int *>(base + off); };
-    int **finals = reinterpret_cast<int **>(base + L.finals);
+    EmbGroups g;
+    g.counts = ip(L.counts);
+    g.keys = reinterpret_cast<int **>(base + L.finals);
+    g.order = g.keys + 1;
+    g.seg = ip(L.seg);
+    g.piece_start = ip(L.pstart);
+    g.piece_seg = ip(L.pseg);
+    g.piece_slot = ip(L.pslot);
+    g.multi_seg = ip(L.mseg);
+    g.multi_slot = ip(L.mslot);
+    g.multi_np = ip(L.mnp);
+    float *partial = reinterpret_cast<float *>(base + L.partial);
     if (!accumulate) {
         const size_t n = static_cast<size_t>(V) * d;
         k_zero_f32<<<4 * di->sms, 256, 0, st>>>(dW, n);
         LCE_CHECK_LAUNCH();
     }
     k_emb_sort<<<1, kEmbSortThreads, 0, st>>>(tokens, static_cast<int>(N), pad_id, V, ip(L.kA), ip(L.vA), ip(L.kB),
-                                               ip(L.vB), ip(L.seg), ip(L.counts), finals, finals + 1);
+                                               ip(L.vB), g);
     LCE_CHECK_LAUNCH();
-    const int64_t segs_max = N;
-    dim3 grid(static_cast<unsigned>(segs_max < 4 * di->sms ? segs_max : 4 * di->sms),
-              static_cast<unsigned>((d + kEmbSegCols - 1) / kEmbSegCols));
+    const unsigned slices = static_cast<unsigned>((d + kEmbSegCols - 1) / kEmbSegCols);
+    const int64_t pmax = emb_pieces_max(N);
+    const dim3 pgrid(static_cast<unsigned>(pmax < 8 * di->sms ? pmax : 8 * di->sms), slices);
     if (dtype == LCE_BF16)
-        k_emb_segsum<__nv_bfloat16><<<grid, kEmbSegCols / 4, 0, st>>>(
-            static_cast<const __nv_bfloat16 *>(dE), finals, finals + 1, ip(L.seg), ip(L.counts), static_cast<int>(d),
-            dW, accumulate ? 1 : 0);
+        k_emb_pieces<__nv_bfloat16><<<pgrid, kEmbSegCols / 4, 0, st>>>(static_cast<const __nv_bfloat16 *>(dE), g,
+                                                                       static_cast<int>(d), dW, partial,
+                                                                       accumulate ? 1 : 0);
     else
-        k_emb_segsum<float><<<grid, kEmbSegCols / 4, 0, st>>>(static_cast<const float *>(dE), finals, finals + 1,
-                                                              ip(L.seg), ip(L.counts), static_cast<int>(d), dW,
-                                                              accumulate ? 1 : 0);
+        k_emb_pieces<float><<<pgrid, kEmbSegCols / 4, 0, st>>>(static_cast<const float *>(dE), g, static_cast<int>(d),
+                                                               dW, partial, accumulate ? 1 : 0);
+    LCE_CHECK_LAUNCH();
+    const int64_t mmax = N / kEmbPiece + 1;
+    const dim3 cgrid(static_cast<unsigned>(mmax < 4 * di->sms ? mmax : 4 * di->sms), slices);
+    k_emb_combine<<<cgrid, kEmbSegCols / 4, 0, st>>>(g, static_cast<int>(d), dW, partial, accumulate ? 1 : 0);
     LCE_CHECK_LAUNCH();
     return LCE_OK;
 }

@@ -15,8 +15,11 @@
 // (8-bit digits; within a 1024-element chunk an element's rank among equal
 // digits comes from a warp match plus per-warp digit offsets, chunks in
 // order), then the list of segment heads (first position of each token).
-// A second kernel sums each segment's rows, a block per (segment, 256-column
-// slice), rows in sorted (= ascending position) order.
+// Segments are cut into pieces of at most kEmbPiece rows (fixed boundaries,
+// so the result does not depend on scheduling). A second kernel sums each
+// piece's rows in order, a block per (piece, 256-column slice): a segment of
+// one piece goes straight into dW, the pieces of a longer segment into fp32
+// partial rows, which a third kernel adds into dW in piece order.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -30,6 +33,25 @@ constexpr int kEmbSortThreads = 1024;
 constexpr int kEmbRadixBits = 8;
 constexpr int kEmbBuckets = 1 << kEmbRadixBits;
 constexpr int kEmbSegCols = 256;   // columns per segment-sum block (64 threads x 4)
+constexpr int kEmbPiece = 64;      // rows per piece of a segment
+
+// Bound on the pieces of N positions and on the partial rows they need.
+__host__ __device__ inline int64_t emb_pieces_max(int64_t N) { return N + N / kEmbPiece + 1; }
+__host__ __device__ inline int64_t emb_slots_max(int64_t N) { return 2 * (N / kEmbPiece) + 2; }
+
+// Grouping output, in the workspace (filled by k_emb_sort).
+struct EmbGroups {
+    int *counts;       // [0] valid positions, [1] segments, [2] pieces, [3] multi-piece segments
+    int **keys;        // -> token of each sorted position
+    int **order;       // -> sorted positions
+    int *seg;          // [nseg + 1] first sorted index of each segment
+    int *piece_start;  // [npieces] first sorted index of the piece
+    int *piece_seg;    // [npieces] its segment
+    int *piece_slot;   // [npieces] partial row, or -1 (single-piece segment: straight into dW)
+    int *multi_seg;    // [nmulti] segments of more than one piece
+    int *multi_slot;   // [nmulti] their first partial row (pieces in order)
+    int *multi_np;     // [nmulti] their piece counts
+};
 
 template <typename T>
 struct Vec4;   // four consecutive elements
@@ -75,9 +97,39 @@ __global__ void __launch_bounds__(256)
 // (N + 1). Out: counts[0] = number of valid positions, counts[1] = number of
 // segments; order = the sorted positions, skey = their tokens, seg[s] = first
 // index of segment s in order (seg[nseg] = count).
+// Block-wide exclusive scan of one int per thread (1024 threads); returns
+// the prefix of this thread and sets *total. Uses warp_incl[32].
+__device__ __forceinline__ int block_scan_1024(int x, int *warp_incl, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) warp_incl[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int v = warp_incl[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += n;
+        }
+        warp_incl[lane] = v;
+    }
+    __syncthreads();
+    const int pre = (warp ? warp_incl[warp - 1] : 0) + incl - x;
+    *total = warp_incl[31];
+    __syncthreads();
+    return pre;
+}
+
 __global__ void __launch_bounds__(kEmbSortThreads)
     k_emb_sort(const int64_t *__restrict__ t, int N, int64_t pad_id, int64_t V, int *kA, int *vA, int *kB, int *vB,
-               int *__restrict__ seg, int *__restrict__ counts, int **final_keys, int **final_vals) {
+               EmbGroups g) {
+    int *seg = g.seg;
+    int *counts = g.counts;
     __shared__ int wcnt[32][kEmbBuckets];   // per-warp digit counts, then per-warp digit offsets
     __shared__ int base[kEmbBuckets];
     __shared__ int ctot[kEmbBuckets];
@@ -205,43 +257,80 @@ __global__ void __launch_bounds__(kEmbSortThreads)
         nseg += warp_incl[31];
         __syncthreads();
     }
+    if (tid == 0) seg[nseg] = nv;
+    __syncthreads();
+
+    // 4. pieces of at most kEmbPiece rows; segments of several pieces get
+    //    consecutive partial rows and an entry in the multi-piece list
+    int npieces = 0, nslots = 0, nmulti = 0;
+    for (int b0 = 0; b0 < nseg; b0 += kEmbSortThreads) {
+        const int sidx = b0 + tid;
+        const int len = sidx < nseg ? seg[sidx + 1] - seg[sidx] : 0;
+        const int np = (len + kEmbPiece - 1) / kEmbPiece;
+        const int multi = np > 1 ? 1 : 0;
+        int tot_p, tot_s, tot_m;
+        const int poff = npieces + block_scan_1024(np, warp_incl, &tot_p);
+        const int soff = nslots + block_scan_1024(multi ? np : 0, warp_incl, &tot_s);
+        const int moff = nmulti + block_scan_1024(multi, warp_incl, &tot_m);
+        for (int k = 0; k < np; ++k) {
+            g.piece_start[poff + k] = seg[sidx] + k * kEmbPiece;
+            g.piece_seg[poff + k] = sidx;
+            g.piece_slot[poff + k] = multi ? soff + k : -1;
+        }
+        if (multi) {
+            g.multi_seg[moff] = sidx;
+            g.multi_slot[moff] = soff;
+            g.multi_np[moff] = np;
+        }
+        npieces += tot_p;
+        nslots += tot_s;
+        nmulti += tot_m;
+    }
     if (tid == 0) {
-        seg[nseg] = nv;
         counts[0] = nv;
         counts[1] = nseg;
-        final_keys[0] = ks;
-        final_vals[0] = vs;
+        counts[2] = npieces;
+        counts[3] = nmulti;
+        g.keys[0] = ks;
+        g.order[0] = vs;
         if (bad_total) atomicOr(&g_status, DEV_TARGET_RANGE);
     }
 }
 
-// dW[v, cols] (+)= sum over the segment's rows, in order; a block per
-// (segment, 256-column slice), four columns per thread, four rows in flight.
+// Sum of one piece's rows in order, four columns per thread, sixteen rows
+// in flight: into dW (single-piece segment; added to dW's value when
+// accumulating) or into the piece's partial row. A block per (piece,
+// 256-column slice).
+constexpr int kEmbRowsInFlight = 16;
 template <typename T>
-__global__ void __launch_bounds__(64, 16)
-    k_emb_segsum(const T *__restrict__ dE, int *const *final_keys, int *const *final_vals, const int *__restrict__ seg,
-                 const int *__restrict__ counts, int d, float *__restrict__ dW, int accumulate) {
-    const int nseg = counts[1];
-    const int *keys = final_keys[0];
-    const int *order = final_vals[0];
+__global__ void __launch_bounds__(64, 8)
+    k_emb_pieces(const T *__restrict__ dE, EmbGroups g, int d, float *__restrict__ dW, float *__restrict__ partial,
+                 int accumulate) {
+    const int npieces = g.counts[2];
+    const int *keys = g.keys[0];
+    const int *order = g.order[0];
     const int col = blockIdx.y * kEmbSegCols + threadIdx.x * 4;
     if (col >= d) return;
-    for (int s = blockIdx.x; s < nseg; s += gridDim.x) {
-        const int j0 = seg[s], j1 = seg[s + 1];
-        float *out = dW + static_cast<int64_t>(keys[j0]) * d + col;
+    for (int p = blockIdx.x; p < npieces; p += gridDim.x) {
+        const int sidx = g.piece_seg[p];
+        const int j0 = g.piece_start[p];
+        const int send = g.seg[sidx + 1];
+        const int j1 = j0 + kEmbPiece < send ? j0 + kEmbPiece : send;
+        const int slot = g.piece_slot[p];
+        float *out = slot < 0 ? dW + static_cast<int64_t>(keys[j0]) * d + col : partial + static_cast<int64_t>(slot) * d + col;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        if (accumulate) {
+        if (slot < 0 && accumulate) {
             const float4 a = *reinterpret_cast<const float4 *>(out);
             acc[0] = a.x, acc[1] = a.y, acc[2] = a.z, acc[3] = a.w;
         }
         int j = j0;
-        for (; j + 4 <= j1; j += 4) {
-            float x[4][4];
+        for (; j + kEmbRowsInFlight <= j1; j += kEmbRowsInFlight) {
+            float x[kEmbRowsInFlight][4];
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
+            for (int r = 0; r < kEmbRowsInFlight; ++r)
                 Vec4<T>::load(dE + static_cast<int64_t>(order[j + r]) * d + col, x[r]);
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
+            for (int r = 0; r < kEmbRowsInFlight; ++r)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) acc[k] += x[r][k];
         }
@@ -250,6 +339,29 @@ __global__ void __launch_bounds__(64, 16)
             Vec4<T>::load(dE + static_cast<int64_t>(order[j]) * d + col, x);
 #pragma unroll
             for (int k = 0; k < 4; ++k) acc[k] += x[k];
+        }
+        *reinterpret_cast<float4 *>(out) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    }
+}
+
+// dW[v] (+)= the partial rows of a multi-piece segment, in piece order.
+__global__ void __launch_bounds__(64, 8)
+    k_emb_combine(EmbGroups g, int d, float *__restrict__ dW, const float *__restrict__ partial, int accumulate) {
+    const int nmulti = g.counts[3];
+    const int *keys = g.keys[0];
+    const int col = blockIdx.y * kEmbSegCols + threadIdx.x * 4;
+    if (col >= d) return;
+    for (int m = blockIdx.x; m < nmulti; m += gridDim.x) {
+        float *out = dW + static_cast<int64_t>(keys[g.seg[g.multi_seg[m]]]) * d + col;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (accumulate) {
+            const float4 a = *reinterpret_cast<const float4 *>(out);
+            acc[0] = a.x, acc[1] = a.y, acc[2] = a.z, acc[3] = a.w;
+        }
+        const float *src = partial + static_cast<int64_t>(g.multi_slot[m]) * d + col;
+        for (int k = 0; k < g.multi_np[m]; ++k) {
+            const float4 a = *reinterpret_cast<const float4 *>(src + static_cast<int64_t>(k) * d);
+            acc[0] += a.x, acc[1] += a.y, acc[2] += a.z, acc[3] += a.w;
         }
         *reinterpret_cast<float4 *>(out) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     }

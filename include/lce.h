@@ -302,14 +302,16 @@ lce_status_t lce_embedding_forward(lce_dtype_t dtype, const void *W, const int64
  * flagged as in the forward). dE [N,d] of `dtype`, dW [V,d] fp32 (device).
  * accumulate = 0 overwrites dW (rows of tokens that do not occur become 0);
  * nonzero adds into it, so for a tied W the output projection's dW (lce_run)
- * and this gradient sum into one buffer. Each row's sum is taken in ascending
- * position order after the positions are grouped by token on the device (the
+ * and this gradient sum into one buffer. The positions are grouped by token
+ * on the device and each row's sum is taken in ascending position order (the
  * batch's per-token gradients aggregated after backward, same page, section
  * 2.2, without atomics): results are reproducible bit for bit.
- * Scratch: lce_embedding_workspace_size(N) bytes of `workspace` (device,
- * 16-byte aligned), or NULL for a stream-ordered allocation.
+ * Long runs of one token are summed in fixed pieces of 64 positions, then the
+ * pieces in order. Scratch: lce_embedding_workspace_size(N, d) bytes of
+ * `workspace` (device, 16-byte aligned), or NULL for a stream-ordered
+ * allocation.
  */
-size_t lce_embedding_workspace_size(int64_t N);
+size_t lce_embedding_workspace_size(int64_t N, int64_t d);
 lce_status_t lce_embedding_backward(lce_dtype_t dtype, const void *dE, const int64_t *tokens, int64_t pad_id,
                                     int64_t N, int64_t d, int64_t V, float *dW, int accumulate, void *workspace,
                                     size_t workspace_bytes, lce_stream_t stream);
