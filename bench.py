@@ -33,14 +33,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel sources it was captured from (sha256 prefix below) and the default
 # vocab chunk, else reported null.
 NCU_TRAFFIC = {"workload": "llama8b", "kernel": "backward", "bytes_per_launch": 1269.0e6,
-               "src_sha256": "611399af09a9378e"}
+               "src_sha256": "9310faeed50c2e46"}
 
 
 def kernel_src_sha256() -> str:
-    import glob
+    """Hash of the sources that define the GEMM kernels (engine and PTX
+    wrappers); the launch configuration is pinned separately (default vocab
+    chunk, no options)."""
     import hashlib
-    files = sorted(glob.glob(os.path.join(ROOT, "chunked_vocab_cross_gb300", "csrc", "*.cu")) +
-                   glob.glob(os.path.join(ROOT, "chunked_vocab_cross_gb300", "csrc", "*.cuh")))
+    files = [os.path.join(ROOT, "chunked_vocab_cross_gb300", "csrc", f) for f in ("lce_gemm.cuh", "tc_ptx.cuh")]
     h = hashlib.sha256()
     for f in files:
         with open(f, "rb") as fh:
@@ -58,23 +59,31 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
-    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    """nvidia-smi clocks and throttle reasons every 50 ms, each sample with its
+    timestamp; summary() keeps the samples inside the window set by mark()
+    (the timed region). Start it a few untimed steps before timing so that
+    nvidia-smi is already sampling when the timed region begins."""
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.window = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "200",
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "50",
                  "-i", str(self.index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
         return self
+
+    def mark(self, t0: float, t1: float):
+        """The timed region, as host wall-clock times (time.time())."""
+        self.window = (t0, t1)
 
     def __exit__(self, *exc):
         self.out = ""
@@ -86,22 +95,37 @@ class ClockSampler:
                 self.proc.kill()
                 self.out, _ = self.proc.communicate()
 
+    @staticmethod
+    def _epoch(stamp: str):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(stamp, fmt).timestamp()
+            except ValueError:
+                continue
+        return None
+
     def summary(self):
         rows = []
         for line in (self.out or "").strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) != 7:
+            if len(parts) != 8:
                 continue
             try:
-                rows.append((float(parts[0]), float(parts[1]), parts[3:]))
+                rows.append((self._epoch(parts[0]), float(parts[1]), float(parts[2]), parts[4:]))
             except ValueError:
                 continue
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clocks unavailable"], "samples": 0}
+        inside = rows
+        if self.window is not None:
+            t0, t1 = self.window
+            inside = [r for r in rows if r[0] is not None and t0 <= r[0] <= t1]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock sample inside the timed region"],
+                    "samples": 0}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({n for _, _, flags in rows for n, f in zip(names, flags) if f.lower() == "active"})
-        return {"sm_mhz": float(np.median([r[0] for r in rows])), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+        reasons = sorted({n for _, _, _, flags in inside for n, f in zip(names, flags) if f.lower() == "active"})
+        return {"sm_mhz": float(np.median([r[1] for r in inside])), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
 
 
 def dist_setup(gpus: int):
@@ -393,11 +417,16 @@ def main():
     torch.cuda.synchronize()
     l0 = lce.launch_count()
     with ClockSampler(local) as clk:
+        for _ in range(3):   # untimed, while the sampler starts
+            step()
+        torch.cuda.synchronize()
+        t_wall0 = time.time()
         ev0.record(stream)
         for _ in range(args.steps):
             step()
         ev1.record(stream)
         torch.cuda.synchronize()
+        clk.mark(t_wall0, time.time())
     barrier(world)
     launches = (lce.launch_count() - l0) // max(1, args.steps) * args.steps
     ms_step = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)

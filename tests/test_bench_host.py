@@ -43,15 +43,23 @@ def test_two_rank_reductions_gloo(tmp_path):
         assert r["tot"] == 3000.0       # whole-job total
 
 
-def test_clock_summary_parsing():
+def test_clock_summary_keeps_samples_inside_the_timed_region():
+    import datetime
+
     import bench
     c = bench.ClockSampler(0)
-    c.out = ("1800, 2070, 1350.5, Not Active, Not Active, Not Active, Active\n"
-             "1900, 2070, 1390.1, Not Active, Not Active, Not Active, Not Active\n"
-             "garbage line\n")
+    c.out = ("2026/12/02 10:00:00.100, 1500, 2070, 1200.0, Not Active, Not Active, Not Active, Not Active\n"
+             "2026/12/02 10:00:00.300, 1800, 2070, 1350.5, Not Active, Not Active, Not Active, Active\n"
+             "2026/12/02 10:00:00.350, 1900, 2070, 1390.1, Not Active, Not Active, Not Active, Not Active\n"
+             "garbage line\n"
+             "2026/12/02 10:00:00.900, 1200, 2070, 900.0, Active, Not Active, Not Active, Not Active\n")
+    t = lambda ms: datetime.datetime(2026, 12, 2, 10, 0, 0, ms * 1000).timestamp()  # noqa: E731
+    c.mark(t(200), t(500))
     s = c.summary()
     assert s["sm_mhz"] == 1850.0 and s["sm_max_mhz"] == 2070.0
     assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 2
+    c.mark(t(600), t(700))
+    assert c.summary()["samples"] == 0
 
 
 def test_reference_arm_other_ranks_exit_silently():
