@@ -33,7 +33,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel sources it was captured from (sha256 prefix below) and the default
 # vocab chunk, else reported null.
 NCU_TRAFFIC = {"workload": "llama8b", "kernel": "backward", "bytes_per_launch": 1269.0e6,
-               "src_sha256": "9310faeed50c2e46"}
+               "src_sha256": "82842a85f2d9a693"}
 
 
 def kernel_src_sha256() -> str:
