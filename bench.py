@@ -32,8 +32,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # from profiles/k_gemm_pair_llama8b_v24k_ncu_full.md; valid only for the
 # kernel sources it was captured from (sha256 prefix below) and the default
 # vocab chunk, else reported null.
-NCU_TRAFFIC = {"workload": "llama8b", "kernel": "backward", "bytes_per_launch": 1269.0e6,
-               "src_sha256": "82842a85f2d9a693"}
+NCU_TRAFFIC = {"workload": "llama8b", "kernel": "backward", "bytes_per_launch": 1247.2e6,
+               "src_sha256": "65ea9b54e89ceb82"}
 
 
 def kernel_src_sha256() -> str:
