@@ -33,19 +33,25 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel sources it was captured from (sha256 prefix below) and the default
 # vocab chunk, else reported null.
 NCU_TRAFFIC = {"workload": "llama8b", "kernel": "backward", "bytes_per_launch": 1247.2e6,
-               "src_sha256": "65ea9b54e89ceb82"}
+               "src_sha256": "0b5117958a93f84b"}
 
 
-def kernel_src_sha256() -> str:
-    """Hash of the sources that define the GEMM kernels (engine and PTX
-    wrappers); the launch configuration is pinned separately (default vocab
-    chunk, no options)."""
+def kernel_src_sha256(texts=None) -> str:
+    """Hash of the code that defines the GEMM kernels (engine and PTX
+    wrappers), with // comments and blank lines removed so that comment edits
+    leave it unchanged; the launch configuration is pinned separately
+    (default vocab chunk, no options). `texts` replaces the files' contents."""
     import hashlib
-    files = [os.path.join(ROOT, "chunked_vocab_cross_gb300", "csrc", f) for f in ("lce_gemm.cuh", "tc_ptx.cuh")]
+    import re
+    if texts is None:
+        texts = []
+        for f in ("lce_gemm.cuh", "tc_ptx.cuh"):
+            with open(os.path.join(ROOT, "chunked_vocab_cross_gb300", "csrc", f), encoding="utf-8") as fh:
+                texts.append(fh.read())
     h = hashlib.sha256()
-    for f in files:
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+    for text in texts:
+        code = [re.sub(r"\s*//.*$", "", line).rstrip() for line in text.splitlines()]
+        h.update("\n".join(line for line in code if line).encode())
     return h.hexdigest()[:16]
 
 

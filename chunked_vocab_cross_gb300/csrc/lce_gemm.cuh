@@ -5,7 +5,8 @@
 // threads per CTA:
 //   warp 0      TMA producer: streams this CTA's 128 A rows and 128 of the
 //               256 B rows per k-block into a 6-stage shared-memory ring
-//               (128-byte swizzle); both CTAs signal the even CTA's barrier.
+//               (5 stages in the fused-optimizer instantiation; 128-byte
+//               swizzle); both CTAs signal the even CTA's barrier.
 //   warp 1      allocates TMEM (512 columns = two 128x256 fp32 accumulators
 //               per CTA); on the even CTA one thread issues
 //               tcgen05.mma.cta_group::2.kind::f16 256x256x16 (bf16 in, fp32
@@ -24,8 +25,11 @@
 //          and stores it (bf16).
 //   T_DW   dW_c = G^T . Hc    (M = chunk vocab rows, K = valid tokens); A and
 //          B are read MN-major straight from G and Hc. With a fused optimizer
-//          the epilogue applies the SGD / AdamW update to those W rows
-//          instead of storing dW (no dW buffer exists).
+//          (KIND_BWD_OPT) the epilogue applies the SGD / AdamW update to those
+//          W rows instead of storing dW (no dW buffer exists): the TMA engine
+//          streams boxes of the rows' weights and optimizer state through a
+//          ring in the warp's staging area, each lane updates its row from
+//          its TMEM gradient, and the boxes are stored back.
 //   T_DH   dHacc (+)= G . W_c (M = valid tokens, K = chunk vocab rows); B is
 //          read MN-major straight from W.
 //

@@ -67,3 +67,11 @@ def test_reference_arm_other_ranks_exit_silently():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
                         "--warmup", "0"], env=env, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_kernel_hash_ignores_comments_only():
+    import bench
+    base = bench.kernel_src_sha256(["int a = 1;\nint b = a; // trailing\n", "asm(\"mov\");\n"])
+    assert base == bench.kernel_src_sha256(["// header\nint a = 1;\n\nint b = a;\n", "asm(\"mov\"); // note\n"])
+    assert base != bench.kernel_src_sha256(["int a = 2;\nint b = a;\n", "asm(\"mov\");\n"])
+    assert len(bench.kernel_src_sha256()) == 16
