@@ -469,3 +469,15 @@ def test_row_gather_gpt1b_shape_bitwise_equal_to_copy_path():
         outs.append((loss, dH, dW))
     for a_, b_ in zip(*outs):
         assert torch.equal(a_, b_)
+
+
+@pytest.mark.parametrize("shape", [(300, 16384, 700), (3, 64, 300001), (131072, 64, 500)],
+                         ids=["large_d", "large_V_tiny_N", "large_N"])
+def test_extreme_shapes(shape):
+    """Shapes at the edges of what the tiles handle: d = 16384 (256 k-blocks
+    per logits tile, 64 d tiles in dW/dH), V = 300001 with 3 tokens (one row
+    block against 1172 vocab tiles, a ragged last tile), and N = 131072 (512
+    row blocks; 128 compaction rounds)."""
+    N, d, V = shape
+    x = make_inputs("gpt1b", N=N, d=d, V=V, padding=("random_frac", 0.2), seqs=1)
+    _run_and_compare(x, vocab_chunk=4096 if V > 4096 else 0)
