@@ -237,3 +237,62 @@ def test_fused_optimizer_sampled_rows_gpt1b():
     err = rel_fro(got - master_old, o["w"] - x.W_f32()[rows])
     print("sampled step err", err)
     assert err <= TOL_REL
+
+
+@pytest.mark.parametrize("case", [
+    ("adamw", "fp32", False, 0.0),   # fp32 W in place: 8 KB ring buffers, fp32 weight boxes
+    ("sgd", "fp32", False, 0.0),     # fp32 W, no state: weight boxes only
+    ("sgd", "bf16", False, 0.9),     # bf16 W in place with a momentum buffer
+    ("sgd", "bf16", True, 0.5),      # fp32 master weights with a momentum buffer
+], ids=lambda c: f"{c[0]}_{c[1]}_{'master' if c[2] else 'inplace'}_m{c[3]}")
+def test_optimizer_state_layouts(case):
+    """Every combination of weights and state the optimizer ring moves (boxes
+    of m, v, fp32 or bf16 weights, bf16 rounding of a master copy), on a
+    ragged V, two steps, against the oracle's own trajectory."""
+    kind, dt, master, momentum = case
+    base = "tiny" if dt == "fp32" else "gpt1b"
+    x = make_inputs(base, N=640, d=136, V=2333, padding=("random_frac", 0.2), seqs=1)
+    assert x.bf16 == (dt == "bf16")
+    H, W, t = to_device(x)
+    # a bf16 W updated in place keeps the update above its rounding (2^-8 |w|)
+    lr = (50.0 if (dt == "bf16" and not master) else 0.5) if kind == "sgd" else 1e-2
+    hp = dict(lr=lr, weight_decay=0.01)
+    if kind == "sgd":
+        opt = lce.FusedOptimizer(W, "sgd", momentum=momentum, master_weights=master, **hp)
+    else:
+        opt = lce.FusedOptimizer(W, "adamw", master_weights=master, **hp)
+    w_or = x.W_f32().astype(np.float64)
+    m_or = v_or = None
+    tol = 3e-3 if dt == "fp32" else TOL_REL
+    for step in (1, 2):
+        w_in = w_or if (dt == "fp32" or master) else _bf16_round(w_or)
+        ref = _oracle_grad(x.H_f32(), _bf16_round(w_or) if dt == "bf16" else w_or, x.targets)
+        kw = dict(hp)
+        if kind == "adamw":
+            kw["eps"] = 10.0 * float(np.max(np.abs(ref["dW"])))
+            opt.eps = kw["eps"]
+        else:
+            kw["momentum"] = momentum
+        old = np64(opt.master if master else W)
+        loss, dH = opt.step(H, t, IGNORE_INDEX, vocab_chunk=768)
+        torch.cuda.synchronize()
+        assert lce.device_status() == 0
+        o = _step(kind, w_in, ref["dW"], step=step, exp_avg=m_or, exp_avg_sq=v_or, **kw)
+        new = np64(opt.master if master else W)
+        bound = tol
+        if dt == "bf16" and not master:   # the in-place bf16 rounding of W
+            bound += 2.0 ** -8 * np.linalg.norm(new) / np.linalg.norm(o["w"] - w_in)
+        errs = {"loss": abs(loss.item() - ref["loss"]), "step": rel_fro(new - old, o["w"] - w_in)}
+        if o["exp_avg"] is not None:
+            errs["m"] = rel_fro(np64(opt.exp_avg), o["exp_avg"])
+        if o["exp_avg_sq"] is not None:
+            errs["v"] = rel_fro(np64(opt.exp_avg_sq), o["exp_avg_sq"])
+        print(case, step, errs, bound)
+        assert errs["loss"] <= (1e-4 if dt == "fp32" else TOL_LOSS), errs
+        assert errs["step"] <= bound, errs
+        assert errs.get("m", 0.0) <= tol and errs.get("v", 0.0) <= 2 * tol, errs
+        if master:
+            assert torch.equal(W, opt.master.to(torch.bfloat16))
+        w_or, m_or, v_or = o["w"], o["exp_avg"], o["exp_avg_sq"]
+        if dt == "bf16" and not master:
+            w_or = _bf16_round(w_or)   # W is stored as the bf16 rounding of the update (the contract)
