@@ -17,9 +17,15 @@
 //   6 k_gemm<BWD>      G_{j+1} = (softmax - onehot)/Nv from recomputed logits
 //                      of chunk j+1, dW[chunk j] = G_j^T Hc and
 //                      dHacc (+)= G_j W[chunk j] (three G buffers; consecutive
-//                      launches overlap through programmatic dependent launch)
+//                      launches overlap through programmatic dependent launch;
+//                      with a fused optimizer, k_gemm<BWD_OPT>: dW tiles of
+//                      chunk j one launch later, applying SGD / AdamW to W,
+//                      four G buffers, launches j = -1 .. chunks)
 //   7 k_dh_scatter     dH = dHacc[inv], zero on ignored rows
-// and finally k_loss_final (loss = sum of the chunks' sums / Nv).
+// and finally k_loss_final (loss = sum of the chunks' sums / Nv). With a
+// stored lse (lse_in), k_lse_from_input replaces steps 3-5.
+// The input-embedding lookup and its gradient (lce_embedding_*) are separate
+// entry points over the kernels of lce_embed.cuh.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
