@@ -229,14 +229,16 @@ class _LinearCrossEntropySplit(torch.autograd.Function):
                 dW.to(W.dtype) if ctx.needs_input_grad[1] else None, None, None)
 
 
-def linear_cross_entropy(H, W, targets, ignore_index: int = -100, fused: bool = True):
+def linear_cross_entropy(H, W, targets, ignore_index: int = -100, fused: bool = False):
     """loss = cross_entropy(H @ W^T, targets, ignore_index) without materialising logits.
 
-    fused=True computes dH and dW during the forward call and keeps them until
-    backward (for a forward that is always followed by backward). fused=False
-    keeps only the per-row lse [N] in forward and runs the gradient passes in
-    backward with the incoming gradient applied on the device: the same total
-    work, split across the two calls, and a forward without gradient work."""
+    fused=False (default) keeps only the per-row lse [N] from forward and runs
+    the gradient passes in backward, the incoming gradient applied inside the
+    kernels; the only elementwise step outside them is the cast of the fp32 dW
+    to a bf16 W's dtype that autograd requires. fused=True computes dH and dW
+    during the forward call and holds them until backward (dW is V x d fp32),
+    then scales them by the incoming gradient with one elementwise pass each;
+    it saves the backward's second compaction (about 0.6% of a step)."""
     if fused:
         return _LinearCrossEntropy.apply(H, W, targets, ignore_index)
     return _LinearCrossEntropySplit.apply(H, W, targets, ignore_index)

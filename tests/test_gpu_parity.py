@@ -186,7 +186,7 @@ def test_autograd_function():
     H, W, t = to_device(x)
     H.requires_grad_(True)
     W.requires_grad_(True)
-    loss = lce.linear_cross_entropy(H, W, t, IGNORE_INDEX)
+    loss = lce.linear_cross_entropy(H, W, t, IGNORE_INDEX, fused=True)
     (2.0 * loss).backward()
     ref = oracle.forward_backward(x.H_f32(), x.W_f32(), x.targets, IGNORE_INDEX)
     assert abs(loss.item() - ref["loss"]) <= TOL_LOSS
