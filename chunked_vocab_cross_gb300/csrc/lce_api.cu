@@ -1105,6 +1105,6 @@ lce_status_t lce_selftest_wait_timeout(int64_t cycles, int32_t *gave_up, lce_str
     return LCE_OK;
 }
 
-int lce_version(void) { return 200; }
+int lce_version(void) { return 300; }
 
 }  // extern "C"
