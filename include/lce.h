@@ -160,7 +160,7 @@ typedef struct {
     const int64_t *targets;   /* [N] */
     int64_t ignore_index;
     int64_t N, d, V;
-    float *loss;              /* required: device fp32 scalar */
+    float *loss;              /* device fp32 scalar; required unless lse_in is given */
     void *dH;                 /* [N,d] of dtype, or NULL for forward only */
     float *dW;                /* [V,d] fp32, or NULL for forward only (NULL iff dH is NULL, except that
                                  dW is NULL with a fused optimizer) */
