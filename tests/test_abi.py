@@ -179,3 +179,30 @@ def test_embedding_entry_points_host_checks_without_gpu(lib):
     assert b(0, 4096, 4096, 0, 10, 64, 100, 4096, 0, 8192, ws - 1, None) == 6   # workspace too small
     # scratch grows with N (grouping the positions) and N/64 partial rows of d, never with V
     assert lib.lce_embedding_workspace_size(16384, 4096) < 16384 * 64 + 2 * (16384 // 64 + 1) * 4096 * 4
+
+
+def test_workspace_relations_across_options(lib):
+    """The workspace of lce_run for each option, against what the layout
+    needs: a fused optimizer holds a fourth G chunk buffer (N_pad * Vc bf16),
+    a token cap bounds scratch by the cap instead of N, fp32 inputs hold
+    split (hi, lo) copies."""
+    def ws(**kw):
+        a = _abi.LceArgs()
+        a.dtype = kw.pop("dtype", 0)
+        a.N, a.d, a.V = kw.pop("N", 5000), kw.pop("d", 1024), kw.pop("V", 50000)
+        a.dH = 4096
+        o = _abi.LceOptim()
+        if kw.pop("optim", False):
+            o.kind = _abi.LCE_OPT_SGD
+            a.optim = ctypes.addressof(o)
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return lib.lce_workspace_size_args(ctypes.byref(a))
+
+    n_pad = (5000 + 255) // 256 * 256
+    assert ws(optim=True) - ws() == n_pad * 6144 * 2                   # one more G buffer, default chunk
+    assert ws(optim=True, vocab_chunk=2048) - ws(vocab_chunk=2048) == n_pad * 2048 * 2
+    capped = ws(N=100000, token_chunk=4096)
+    assert abs(capped - ws(N=200000, token_chunk=4096)) < 4096         # only the per-chunk loss sums grow
+    assert capped < ws(N=100000) / 10
+    assert ws(dtype=1) > ws() + 2 * 50000 * 1024 * 2                   # split copy of W (hi + lo)
