@@ -400,7 +400,7 @@ def main():
                   row_gather=args.row_gather)
         if opt is not None:
             opt.step_count += 1
-            kw["optim"] = opt._optim()
+            kw["optim"] = opt.optim_args()
         if args.two_call:
             # forward storing lse, then the backward alone from it
             lce.lce_run(Hx, W, tx, -100, loss=lx, lse=lse_buf, **kw)

@@ -273,7 +273,9 @@ class FusedOptimizer:
         self.exp_avg_sq = z() if algorithm == "adamw" else None
         self.master = W.float() if master_weights else None
 
-    def _optim(self) -> "_abi.LceOptim":
+    def optim_args(self) -> "_abi.LceOptim":
+        """The lce_optim_t of the next update (the step count as it stands),
+        for a direct lce_run(..., optim=...) call."""
         o = _abi.LceOptim()
         o.kind = _abi.LCE_OPT_ADAMW if self.algorithm == "adamw" else _abi.LCE_OPT_SGD
         o.lr, o.weight_decay, o.momentum = self.lr, self.weight_decay, self.momentum
@@ -295,7 +297,7 @@ class FusedOptimizer:
         dH = torch.empty_like(H)
         try:
             lce_run(H, self.W, targets, ignore_index, loss=loss, dH=dH, grad_scale=grad_scale, grad_loss=grad_loss,
-                    lse_in=lse_in, vocab_chunk=vocab_chunk, workspace=workspace, optim=self._optim(),
+                    lse_in=lse_in, vocab_chunk=vocab_chunk, workspace=workspace, optim=self.optim_args(),
                     stream=stream)
         except Exception:
             self.step_count -= 1

@@ -77,7 +77,7 @@ def _adamw_run(H, W, t, row_gather, master):
         loss = torch.empty((), dtype=torch.float32, device="cuda")
         dH = torch.empty_like(H)
         opt.step_count += 1
-        lce.lce_run(H, Wc, t, IGNORE_INDEX, loss=loss, dH=dH, vocab_chunk=1024, optim=opt._optim(),
+        lce.lce_run(H, Wc, t, IGNORE_INDEX, loss=loss, dH=dH, vocab_chunk=1024, optim=opt.optim_args(),
                     row_gather=row_gather)
         outs += [loss, dH]
     torch.cuda.synchronize()
