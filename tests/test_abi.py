@@ -206,3 +206,19 @@ def test_workspace_relations_across_options(lib):
     assert abs(capped - ws(N=200000, token_chunk=4096)) < 4096         # only the per-chunk loss sums grow
     assert capped < ws(N=100000) / 10
     assert ws(dtype=1) > ws() + 2 * 50000 * 1024 * 2                   # split copy of W (hi + lo)
+
+
+def test_binding_arity_matches_header():
+    """Each function's parameter count in include/lce.h equals the length of
+    its ctypes argtypes (a mismatch would shift every later argument)."""
+    import re
+    text = open(os.path.join(INCLUDE, "lce.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    decls = re.findall(r"\b(?:lce_status_t|size_t|int|int64_t|const char \*)\s*(lce_\w+)\s*\(([^)]*)\)\s*;", text)
+    assert decls
+    for name, params in decls:
+        params = params.strip()
+        n = 0 if params in ("", "void") else params.count(",") + 1
+        assert name in _abi.SIGNATURES, name
+        assert len(_abi.SIGNATURES[name][1]) == n, (name, n, len(_abi.SIGNATURES[name][1]))
+    assert {d[0] for d in decls} == set(_abi.SIGNATURES)
