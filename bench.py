@@ -246,9 +246,9 @@ def run_embedding(args):
     tok = np.where(x.targets == -100, pad, x.targets)
     nv = int((tok != pad).sum())
     distinct = int(np.unique(tok[tok != pad]).size)
-    W = torch.from_numpy(x.W.view(np.int16)).view(torch.bfloat16).cuda()
+    W = host_tensors(x)[1].cuda()
     t = torch.from_numpy(tok).cuda()
-    dE = torch.randn(w.N, w.d, device="cuda").to(torch.bfloat16)
+    dE = torch.randn(w.N, w.d, device="cuda").to(W.dtype)
     dW = torch.zeros(w.V, w.d, dtype=torch.float32, device="cuda")
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")   # 256 MB > L2, written between steps
 
@@ -270,19 +270,30 @@ def run_embedding(args):
         ms.append(e0.elapsed_time(e1))
     status = lce.device_status()
     med = float(np.median(ms))
-    bytes_alg = nv * w.d * 2 + w.N * w.d * 2 + nv * w.d * 2 + distinct * w.d * 8
+    elt = W.element_size()
+    bytes_alg = nv * w.d * elt + w.N * w.d * elt + nv * w.d * elt + distinct * w.d * 8
     peaks, src = load_peaks()
     peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     gbs = bytes_alg / (med / 1e3) / 1e9
     print(json.dumps({
         "metric": "input-embedding lookup + gradient (tied W), tokens/s", "value": w.N / (med / 1e3),
         "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": med,
-        "higher_is_better": True, "dtype": "bf16 (fp32 dW)", "data": "synthetic",
+        "higher_is_better": True, "dtype": ("bf16" if x.bf16 else "f32") + " (fp32 dW)", "data": "synthetic",
         "config": {"workload": w.name, "N": w.N, "d": w.d, "V": w.V, "valid": nv, "distinct_tokens": distinct,
                    "l2": "256 MB buffer written between steps"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                      "traffic": None, "peak_kind": f"hbm_gbs ({src})", "bytes_per_step": bytes_alg},
         "device_status": status}), flush=True)
+
+
+def host_tensors(x):
+    """(H, W) of a synthetic batch as CPU torch tensors of the workload's
+    dtype: bf16 bit patterns reinterpreted, fp32 arrays as they are."""
+    import torch
+    if x.bf16:
+        return (torch.from_numpy(x.H.view(np.int16)).view(torch.bfloat16),
+                torch.from_numpy(x.W.view(np.int16)).view(torch.bfloat16))
+    return torch.from_numpy(x.H), torch.from_numpy(x.W)
 
 
 def eager_context(H, W, t, nv, steps):
@@ -380,16 +391,18 @@ def main():
     x = make_inputs(args.workload, **over)
     nv = int((x.targets != -100).sum())
     w = x.workload
-    H_host = torch.from_numpy(x.H.view(np.int16)).view(torch.bfloat16).pin_memory()
+    H_cpu, W_cpu = host_tensors(x)
+    H_host = H_cpu.pin_memory()
     t_host = torch.from_numpy(x.targets).pin_memory()
     H = H_host.to(dev)
-    W = torch.from_numpy(x.W.view(np.int16)).view(torch.bfloat16).to(dev)
+    W = W_cpu.to(dev)
     t = t_host.to(dev)
     loss = torch.empty((), dtype=torch.float32, device=dev)
     dH = torch.empty_like(H)
     fused = args.optim != "none"
     dW = None if fused else torch.empty(W.shape, dtype=torch.float32, device=dev)
-    ws = torch.empty(lce.workspace_size(w.N, w.d, w.V, vocab_chunk=args.vocab_chunk, token_chunk=args.token_chunk,
+    ws = torch.empty(lce.workspace_size(w.N, w.d, w.V, dtype=W.dtype, vocab_chunk=args.vocab_chunk,
+                                        token_chunk=args.token_chunk,
                                         fused_optimizer=fused, row_gather=args.row_gather),
                      dtype=torch.uint8, device=dev)
     lse_buf = torch.empty(w.N, dtype=torch.float32, device=dev) if args.two_call else None
@@ -521,7 +534,8 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_step, "ms_per_step_median": float(np.median(step_ms)),
         "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "bf16" if x.bf16 else "f32 (bf16 hi/lo split products)",
+        "data": "synthetic",
         "config": workload_desc(x, nv),
         "pct_dense_bf16_peak": {
             "useful_tflops": tflops_useful,
@@ -536,7 +550,7 @@ def main():
         "phase_share": {k: (v["ms"] / total_prof if total_prof else None) for k, v in phases.items()},
         "cpu_baseline": cpu,
         "e2e": {"value": nv / (e2e_ms / 1e3) * world, "unit": UNIT,
-                "h2d_bytes_per_step": int(H.numel() * 2 + t.numel() * 8), "d2h_bytes_per_step": 4,
+                "h2d_bytes_per_step": int(H.numel() * H.element_size() + t.numel() * 8), "d2h_bytes_per_step": 4,
                 "resident": "W (weights)", "ms_per_step": e2e_ms},
         "gpu_launches": int(launches),
         "device_status": status,

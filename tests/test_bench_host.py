@@ -75,3 +75,17 @@ def test_kernel_hash_ignores_comments_only():
     assert base == bench.kernel_src_sha256(["// header\nint a = 1;\n\nint b = a;\n", "asm(\"mov\"); // note\n"])
     assert base != bench.kernel_src_sha256(["int a = 2;\nint b = a;\n", "asm(\"mov\");\n"])
     assert len(bench.kernel_src_sha256()) == 16
+
+
+def test_host_tensors_follow_the_workload_dtype():
+    import torch
+
+    import bench
+    from synth_inputs import bf16_bits_to_f32, make_inputs
+    x = make_inputs("tiny", N=8, d=16, V=20)
+    H, W = bench.host_tensors(x)
+    assert H.dtype == torch.float32 and H.shape == (8, 16) and torch.equal(H, torch.from_numpy(x.H))
+    y = make_inputs("gpt1b", N=8, d=16, V=20, seqs=1)
+    H, W = bench.host_tensors(y)
+    assert H.dtype == torch.bfloat16 and W.shape == (20, 16)
+    assert torch.equal(H.float(), torch.from_numpy(bf16_bits_to_f32(y.H)))
