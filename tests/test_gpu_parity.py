@@ -481,3 +481,26 @@ def test_extreme_shapes(shape):
     N, d, V = shape
     x = make_inputs("gpt1b", N=N, d=d, V=V, padding=("random_frac", 0.2), seqs=1)
     _run_and_compare(x, vocab_chunk=4096 if V > 4096 else 0)
+
+
+@pytest.mark.parametrize("shape", [(300, 64, 50257, ("random_frac", 0.2)), (200, 64, 262144 - 57, ("random_frac", 0.1)),
+                                   (129, 64, 1000, ("none",))],
+                         ids=["V50257", "V262087", "Nv129"])
+def test_tail_shapes(shape):
+    """Vocabulary sizes that are not multiples of the 256-wide tiles (GPT-2's
+    50257 and 2^18 - 57) and a valid count one past a 128-row boundary."""
+    N, d, V, pad = shape
+    x = make_inputs("gpt1b", N=N, d=d, V=V, padding=pad, seqs=1)
+    if pad == ("none",):
+        assert int((x.targets != IGNORE_INDEX).sum()) == N
+    _run_and_compare(x, vocab_chunk=4096)
+
+
+@pytest.mark.parametrize("shape", [(100, 64, 50257), (300, 72, 1000)], ids=["V50257", "d72"])
+def test_fp32_tail_shapes(shape):
+    """The split-precision path on a GPT-2-sized ragged vocabulary and on a d
+    that is not a multiple of 64 (per-block MN-major boxes)."""
+    N, d, V = shape
+    x = make_inputs("tiny", N=N, d=d, V=V, padding=("random_frac", 0.1))
+    errs = _run_and_compare(x, vocab_chunk=4096)
+    assert errs["loss"] <= 1e-4 and errs["dH"] <= 1e-3 and errs["dW"] <= 1e-3, errs
