@@ -33,7 +33,12 @@ not a reordering of the arithmetic). Each row's max and log-sum-exp are taken
 over the complete row of V logits, never by the streaming recurrence the fast
 path uses.
 
-Pins (tests/test_oracle_pins.py): closed forms at W=0, H=0, V=1 and V=2,
+The same definition is written a second time as plain C++ loops
+(oracle/lce_oracle.cpp, loaded through oracle/cpp_oracle.py); the two share
+nothing but the definition, and tests/test_oracle_cross.py checks that they
+agree to rounding.
+
+Pins (tests/test_oracle_pins.py, run against both): closed forms at W=0, H=0, V=1 and V=2,
 central finite differences on tiny inputs, float64 torch autograd of
 cross_entropy(H @ W.T), and invariants (rows of G sum to zero so the columns of
 dW sum to zero; shifting every vocab row by the same vector changes nothing;
@@ -45,7 +50,7 @@ import numpy as np
 
 __all__ = [
     "valid_rows", "out_of_range_targets", "forward", "forward_backward",
-    "lse_rows", "sampled_reference",
+    "sampled_reference",
 ]
 
 _ROW_BATCH = 256      # rows of H per matmul call
@@ -98,16 +103,6 @@ def _check(H, W, targets, ignore_index):
     if bad:
         raise ValueError(f"{bad} targets outside [0, V) that are not ignore_index")
     return H, W, t
-
-
-def lse_rows(H, W, rows) -> np.ndarray:
-    """lse_i for the given row indices of H (float64)."""
-    rows = np.asarray(rows, dtype=np.int64)
-    out = np.empty(rows.shape[0], dtype=np.float64)
-    for b0 in range(0, rows.shape[0], _ROW_BATCH):
-        r = rows[b0:b0 + _ROW_BATCH]
-        out[b0:b0 + r.shape[0]] = _lse(_logits(_f64(H[r]), W))
-    return out
 
 
 def forward(H, W, targets, ignore_index: int = -100) -> dict:

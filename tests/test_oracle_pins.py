@@ -1,9 +1,13 @@
-"""Pins for the fp64 oracle against facts fixed by the definition and by
-mathematics, not by the oracle itself: closed forms, a hand-derived worked
+"""Pins for the fp64 oracles against facts fixed by the definition and by
+mathematics, not by the oracles themselves: closed forms, a hand-derived worked
 example, central finite differences, an independent library autograd, and
-invariants. Each is chosen so that a plausible slip in the oracle (a dropped
+invariants. Each is chosen so that a plausible slip in an oracle (a dropped
 -onehot term, the wrong normaliser, a transposed operand, a wrong index or sign)
-fails at least one of them."""
+fails at least one of them.
+
+The loss-path pins run against both implementations of the definition: the
+plain C++ one (oracle/lce_oracle.cpp, loops and std::thread) and the numpy one
+(oracle/lce_oracle.py, library matmuls), through the ``lo`` fixture."""
 import json
 import math
 import os
@@ -12,9 +16,16 @@ import numpy as np
 import pytest
 
 import oracle
+from oracle import cpp_oracle
 from synth_inputs import IGNORE_INDEX
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(params=["cpp", "numpy"])
+def lo(request):
+    """The loss-path oracle under test: the C++ one or the numpy one."""
+    return cpp_oracle if request.param == "cpp" else oracle
 
 
 def _rand(N, d, V, seed=0, pad=0.25, scale=1.0):
@@ -28,10 +39,10 @@ def _rand(N, d, V, seed=0, pad=0.25, scale=1.0):
 
 # ---------------------------------------------------------------- closed forms
 
-def test_zero_W_gives_ln_V_and_closed_form_dW():
+def test_zero_W_gives_ln_V_and_closed_form_dW(lo):
     H, _, t = _rand(37, 5, 11, seed=1)
     W = np.zeros((11, 5))
-    r = oracle.forward_backward(H, W, t)
+    r = lo.forward_backward(H, W, t)
     valid = t != IGNORE_INDEX
     nv = valid.sum()
     assert r["loss"] == pytest.approx(math.log(11), abs=1e-14)
@@ -43,10 +54,10 @@ def test_zero_W_gives_ln_V_and_closed_form_dW():
     np.testing.assert_array_equal(r["dH"], 0.0)
 
 
-def test_zero_H_gives_ln_V_and_closed_form_dH():
+def test_zero_H_gives_ln_V_and_closed_form_dH(lo):
     _, W, t = _rand(29, 4, 7, seed=2)
     H = np.zeros((29, 4))
-    r = oracle.forward_backward(H, W, t)
+    r = lo.forward_backward(H, W, t)
     valid = t != IGNORE_INDEX
     nv = valid.sum()
     assert r["loss"] == pytest.approx(math.log(7), abs=1e-14)
@@ -57,16 +68,16 @@ def test_zero_H_gives_ln_V_and_closed_form_dH():
     np.testing.assert_array_equal(r["dW"], 0.0)
 
 
-def test_single_class_gives_zero():
+def test_single_class_gives_zero(lo):
     H, W, _ = _rand(9, 3, 1, seed=3)
     t = np.array([0, 0, IGNORE_INDEX, 0, 0, 0, IGNORE_INDEX, 0, 0])
-    r = oracle.forward_backward(H, W, t)
+    r = lo.forward_backward(H, W, t)
     assert r["loss"] == 0.0
     np.testing.assert_array_equal(r["dH"], 0.0)
     np.testing.assert_array_equal(r["dW"], 0.0)
 
 
-def test_two_class_softplus_closed_form():
+def test_two_class_softplus_closed_form(lo):
     # d = 1, V = 2: loss_i = softplus(s_other - s_target), a logistic loss
     g = np.random.default_rng(4)
     N = 13
@@ -74,7 +85,7 @@ def test_two_class_softplus_closed_form():
     W = np.array([[0.7], [-1.3]])
     t = g.integers(0, 2, N)
     t[[2, 5]] = IGNORE_INDEX
-    r = oracle.forward_backward(H, W, t)
+    r = lo.forward_backward(H, W, t)
     valid = np.nonzero(t != IGNORE_INDEX)[0]
     nv = len(valid)
     loss = 0.0
@@ -94,14 +105,14 @@ def test_two_class_softplus_closed_form():
     np.testing.assert_allclose(r["dW"], dW, rtol=1e-13, atol=1e-16)
 
 
-def test_hand_derived_worked_example():
+def test_hand_derived_worked_example(lo):
     with open(os.path.join(GOLDEN, "worked_example_3x3.json")) as f:
         ex = json.load(f)
     ln2, ln3 = math.log(2), math.log(3)
     H = np.array(ex["H"], dtype=float)
     W = np.array([[0, 0], [ln2, 0], [0, ln3]])
     t = np.array(ex["targets"])
-    r = oracle.forward_backward(H, W, t, ex["ignore_index"])
+    r = lo.forward_backward(H, W, t, ex["ignore_index"])
     assert r["loss"] == pytest.approx(math.log(20) / 3, rel=1e-15)
     np.testing.assert_allclose(np.exp(r["lse"]), [4, 5, 6], rtol=1e-15)
     dH = np.array([[-ln2 / 2, ln3 / 4], [ln2 / 5, 3 * ln3 / 5], [ln2 / 3, -ln3 / 2], [0, 0]]) / 3
@@ -113,10 +124,10 @@ def test_hand_derived_worked_example():
     assert np.all(r["dH"][3] == 0.0)
 
 
-def test_no_valid_rows_gives_nan_loss_and_zero_grads():
+def test_no_valid_rows_gives_nan_loss_and_zero_grads(lo):
     H, W, _ = _rand(6, 3, 4, seed=5)
     t = np.full(6, IGNORE_INDEX)
-    r = oracle.forward_backward(H, W, t)
+    r = lo.forward_backward(H, W, t)
     assert math.isnan(r["loss"])
     np.testing.assert_array_equal(r["dH"], 0.0)
     np.testing.assert_array_equal(r["dW"], 0.0)
@@ -125,23 +136,23 @@ def test_no_valid_rows_gives_nan_loss_and_zero_grads():
 
 # ---------------------------------------------------------- finite differences
 
-def _loss_only(H, W, t):
-    return oracle.forward(H, W, t)["loss"]
+def _loss_only(lo, H, W, t):
+    return lo.forward(H, W, t)["loss"]
 
 
-def test_central_finite_differences():
+def test_central_finite_differences(lo):
     H, W, t = _rand(4, 3, 5, seed=6, pad=0.0)
     t[1] = IGNORE_INDEX
-    r = oracle.forward_backward(H, W, t)
+    r = lo.forward_backward(H, W, t)
     eps = 1e-6
     for A, grad in ((H, r["dH"]), (W, r["dW"])):
         num = np.zeros_like(A)
         for idx in np.ndindex(A.shape):
             old = A[idx]
             A[idx] = old + eps
-            lp = _loss_only(H, W, t)
+            lp = _loss_only(lo, H, W, t)
             A[idx] = old - eps
-            lm = _loss_only(H, W, t)
+            lm = _loss_only(lo, H, W, t)
             A[idx] = old
             num[idx] = (lp - lm) / (2 * eps)
         np.testing.assert_allclose(grad, num, atol=2e-9)
@@ -150,13 +161,13 @@ def test_central_finite_differences():
 # --------------------------------------------------- independent library check
 
 @pytest.mark.parametrize("shape", [(1, 1, 2), (7, 3, 5), (64, 16, 33), (200, 24, 300)])
-def test_torch_float64_autograd(shape):
+def test_torch_float64_autograd(lo, shape):
     torch = pytest.importorskip("torch")
     N, d, V = shape
     H, W, t = _rand(N, d, V, seed=N + d + V, scale=2.0)
     if N > 1:
         t[0] = IGNORE_INDEX
-    r = oracle.forward_backward(H, W, t)
+    r = lo.forward_backward(H, W, t)
     Ht = torch.tensor(H, requires_grad=True)
     Wt = torch.tensor(W, requires_grad=True)
     loss = torch.nn.functional.cross_entropy(Ht @ Wt.T, torch.tensor(t), ignore_index=IGNORE_INDEX)
@@ -166,12 +177,12 @@ def test_torch_float64_autograd(shape):
     np.testing.assert_allclose(r["dW"], Wt.grad.numpy(), rtol=1e-10, atol=1e-15)
 
 
-def test_torch_float64_autograd_tiny_workload():
+def test_torch_float64_autograd_tiny_workload(lo):
     torch = pytest.importorskip("torch")
     from synth_inputs import make_inputs
     x = make_inputs("tiny")
     H, W = x.H.astype(np.float64), x.W.astype(np.float64)
-    r = oracle.forward_backward(H, W, x.targets)
+    r = lo.forward_backward(H, W, x.targets)
     Ht = torch.tensor(H, requires_grad=True)
     Wt = torch.tensor(W, requires_grad=True)
     loss = torch.nn.functional.cross_entropy(Ht @ Wt.T, torch.tensor(x.targets), ignore_index=IGNORE_INDEX)
@@ -184,92 +195,98 @@ def test_torch_float64_autograd_tiny_workload():
 
 # ------------------------------------------------------------------ invariants
 
-def test_columns_of_dW_sum_to_zero():
+def test_columns_of_dW_sum_to_zero(lo):
     H, W, t = _rand(50, 6, 17, seed=7, scale=3.0)
-    r = oracle.forward_backward(H, W, t)
+    r = lo.forward_backward(H, W, t)
     np.testing.assert_allclose(r["dW"].sum(0), 0.0, atol=1e-15)
 
 
-def test_common_shift_of_vocab_rows_changes_nothing():
+def test_common_shift_of_vocab_rows_changes_nothing(lo):
     H, W, t = _rand(40, 5, 9, seed=8)
     c = np.random.default_rng(9).standard_normal(5)
-    a = oracle.forward_backward(H, W, t)
-    b = oracle.forward_backward(H, W + c[None, :], t)
+    a = lo.forward_backward(H, W, t)
+    b = lo.forward_backward(H, W + c[None, :], t)
     assert a["loss"] == pytest.approx(b["loss"], rel=1e-12)
     np.testing.assert_allclose(a["dH"], b["dH"], atol=1e-14)
     np.testing.assert_allclose(a["dW"], b["dW"], atol=1e-14)
 
 
-def test_token_permutation():
+def test_token_permutation(lo):
     H, W, t = _rand(31, 4, 10, seed=10)
     p = np.random.default_rng(11).permutation(31)
-    a = oracle.forward_backward(H, W, t)
-    b = oracle.forward_backward(H[p], W, t[p])
+    a = lo.forward_backward(H, W, t)
+    b = lo.forward_backward(H[p], W, t[p])
     assert a["loss"] == pytest.approx(b["loss"], rel=1e-13)
     np.testing.assert_allclose(a["dH"][p], b["dH"], atol=1e-15)
     np.testing.assert_allclose(a["dW"], b["dW"], atol=1e-15)
 
 
-def test_padded_rows_are_exact_zero_and_removable():
+def test_padded_rows_are_exact_zero_and_removable(lo):
     H, W, t = _rand(30, 4, 8, seed=12, pad=0.4)
-    a = oracle.forward_backward(H, W, t)
+    a = lo.forward_backward(H, W, t)
     pad = t == IGNORE_INDEX
     assert pad.any()
     assert np.all(a["dH"][pad] == 0.0)
-    b = oracle.forward_backward(H[~pad], W, t[~pad])
+    b = lo.forward_backward(H[~pad], W, t[~pad])
     assert a["loss"] == pytest.approx(b["loss"], rel=1e-14)
     np.testing.assert_allclose(a["dH"][~pad], b["dH"], atol=1e-16)
     np.testing.assert_allclose(a["dW"], b["dW"], atol=1e-16)
     # padded rows' H values must not matter at all
     H2 = H.copy()
     H2[pad] = 1e6
-    c = oracle.forward_backward(H2, W, t)
+    c = lo.forward_backward(H2, W, t)
     np.testing.assert_array_equal(a["dW"], c["dW"])
 
 
-def test_normaliser_is_valid_count_not_N():
+def test_normaliser_is_valid_count_not_N(lo):
     H, W, t = _rand(20, 3, 6, seed=13, pad=0.0)
     t[:10] = IGNORE_INDEX
-    r = oracle.forward_backward(H, W, t)
+    r = lo.forward_backward(H, W, t)
     assert r["loss"] == pytest.approx(r["loss_rows"].mean(), rel=1e-14)
     assert r["n_valid"] == 10
 
 
 # --------------------------------------------------------------- compaction
 
-def test_compaction_golden_cases():
+def test_compaction_golden_cases(lo):
     with open(os.path.join(GOLDEN, "compaction_small.json")) as f:
         cases = json.load(f)["cases"]
     for c in cases:
         t = np.array(c["targets"], dtype=np.int64)
-        assert oracle.valid_rows(t, c["ignore_index"]).tolist() == c["valid"]
+        assert lo.valid_rows(t, c["ignore_index"]).tolist() == c["valid"]
+        # the numpy oracle counts out-of-range targets; the C++ one refuses them
         assert oracle.out_of_range_targets(t, c["ignore_index"], c["V"]) == c["out_of_range"]
+        if c["out_of_range"]:
+            with pytest.raises(ValueError):
+                cpp_oracle.valid_rows(t, c["ignore_index"], c["V"])
+        else:
+            assert cpp_oracle.valid_rows(t, c["ignore_index"], c["V"]).tolist() == c["valid"]
 
 
-def test_compaction_brute_force():
+def test_compaction_brute_force(lo):
     g = np.random.default_rng(14)
     for n in (0, 1, 31, 32, 33, 1000, 4097):
         t = g.integers(-3, 5, n)
         t[g.random(n) < 0.3] = IGNORE_INDEX
         expect = [i for i in range(n) if t[i] != IGNORE_INDEX]
-        assert oracle.valid_rows(t, IGNORE_INDEX).tolist() == expect
+        assert lo.valid_rows(t, IGNORE_INDEX).tolist() == expect
 
 
-def test_out_of_range_target_is_refused():
+def test_out_of_range_target_is_refused(lo):
     H, W, t = _rand(5, 2, 3, seed=15, pad=0.0)
     t[2] = 3
     with pytest.raises(ValueError):
-        oracle.forward_backward(H, W, t)
+        lo.forward_backward(H, W, t)
 
 
 # ------------------------------------------------------- sampled reference
 
-def test_sampled_reference_matches_full():
+def test_sampled_reference_matches_full(lo):
     H, W, t = _rand(300, 8, 70, seed=16, scale=2.0)
-    full = oracle.forward_backward(H, W, t)
+    full = lo.forward_backward(H, W, t)
     rows = np.array([0, 5, 17, 299, 123])
     vocab = np.array([0, 69, 33, 1])
-    s = oracle.sampled_reference(H, W, t, IGNORE_INDEX, rows, vocab)
+    s = lo.sampled_reference(H, W, t, IGNORE_INDEX, rows, vocab)
     assert s["loss"] == pytest.approx(full["loss"], rel=1e-13)
     np.testing.assert_allclose(s["dH_rows"], full["dH"][rows], atol=1e-15)
     np.testing.assert_allclose(s["dW_rows"], full["dW"][vocab], atol=1e-15)
