@@ -29,9 +29,9 @@ METRIC = "fused linear-CE fwd+bwd valid tokens/sec; % of dense BF16 tensor peak"
 UNIT = "valid tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # DRAM bytes (read + write) per backward k_gemm launch of the llama8b shape,
-# from profiles/k_gemm_pair_llama8b_v24k_ncu_full.md; valid only for the
-# kernel sources it was captured from (sha256 prefix below) and the default
-# vocab chunk, else reported null.
+# from an ncu capture of a reduced-V case with the same per-launch tile
+# counts; valid only for the kernel sources it was captured from (sha256
+# prefix below) and the default vocab chunk, else reported null.
 NCU_TRAFFIC = {"workload": "llama8b", "kernel": "backward", "bytes_per_launch": 1247.2e6,
                "src_sha256": "0b5117958a93f84b"}
 
@@ -172,24 +172,41 @@ def sum_over_ranks(x: float, world: int, device: str = "cuda") -> float:
     return float(t.item())
 
 
+def _oracle_rows(x, rows: int):
+    """H rows and targets of the first `rows` valid positions (as stored:
+    bf16 bit patterns or fp32), the oracle's input for a sample."""
+    valid = np.nonzero(x.targets != -100)[0][:rows]
+    return np.ascontiguousarray(x.H[valid]), np.ascontiguousarray(x.targets[valid])
+
+
+def cpu_oracle_time(x, rows: int, threads: int) -> float:
+    """Seconds the plain C++ fp64 oracle, as it stands, takes for the
+    forward + backward of the first `rows` valid rows of the batch over the
+    full V and d (their loss, their dH rows and their contribution to every
+    dW row), on `threads` host threads."""
+    from oracle import cpp_oracle
+    Hs, ts = _oracle_rows(x, rows)
+    t0 = time.perf_counter()
+    cpp_oracle.forward_backward(Hs, x.W, ts, -100, threads=threads, bf16=x.bf16)
+    return time.perf_counter() - t0
+
+
+def cpu_oracle_sample_rows(x, budget_s: float, threads: int) -> int:
+    """Rows of a sample that takes about `budget_s` (from a timed 16-row run)."""
+    nv = int((x.targets != -100).sum())
+    r0 = min(16, nv)
+    t0 = cpu_oracle_time(x, r0, threads)
+    return int(max(r0, min(nv, round(budget_s / max(t0, 1e-6) * r0))))
+
+
 def cpu_oracle_rate(x, budget_s: float):
-    """The fp64 oracle, as it stands, on the first valid rows of the batch
-    (full V and d, forward + backward), grown batch by batch until `budget_s`."""
-    import oracle
-    valid = np.nonzero(x.targets != -100)[0]
-    # input preparation, outside the timed loop: exact float64 copies of H and W
-    H = x.H_f32()[valid[:8192]].astype(np.float64)
-    W = x.W_f32().astype(np.float64)
-    tv = x.targets[valid[:8192]]
-    rows, t0, step = 0, time.perf_counter(), 128
-    while rows < len(tv):
-        oracle.forward_backward(H[rows:rows + step], W, tv[rows:rows + step], -100)
-        rows += len(tv[rows:rows + step])
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    el = time.perf_counter() - t0
-    cores = len(os.sched_getaffinity(0))
-    return rows / el, el, rows, cores
+    """The C++ oracle's rate in valid tokens/s on a bounded sample of the
+    batch (about `budget_s` of work), with the thread count it used."""
+    from oracle import cpp_oracle
+    threads = cpp_oracle.default_threads()
+    rows = cpu_oracle_sample_rows(x, budget_s, threads)
+    el = cpu_oracle_time(x, rows, threads)
+    return rows / el, el, rows, threads
 
 
 def workload_desc(x, nv):
@@ -201,30 +218,75 @@ def workload_desc(x, nv):
 
 
 def run_reference(args):
+    """The reference arm: the plain C++ fp64 oracle on the host cores. One
+    step = the oracle's forward + backward of the first R valid rows of the
+    batch over the full V and d (R sized so a step takes about
+    LCE_REF_STEP_S seconds, default 6); ms_per_step is the timed step."""
     rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
     if rank != 0:
         return
+    from oracle import cpp_oracle
     from synth_inputs import make_inputs
     x = make_inputs(args.workload)
     nv = int((x.targets != -100).sum())
+    threads = cpp_oracle.default_threads()
     budget = float(os.environ.get("LCE_REF_STEP_S", "6"))
-    times, rows_done = [], 0
+    rows = cpu_oracle_sample_rows(x, budget, threads)
     for _ in range(args.warmup):
-        cpu_oracle_rate(x, budget / 4)
-    for _ in range(args.steps):
-        rate, el, rows, cores = cpu_oracle_rate(x, budget)
-        times.append(el)
-        rows_done += rows
-    value = rows_done / sum(times)
+        cpu_oracle_time(x, min(16, rows), threads)
+    times = [cpu_oracle_time(x, rows, threads) for _ in range(args.steps)]
+    ms_step = 1e3 * float(np.mean(times))
+    value = rows / (ms_step / 1e3)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * nv / value,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "ms_per_step_median": 1e3 * float(np.median(times)),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_desc(x, nv),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"each step: the first valid rows of the batch (about {budget:.0f} s of "
-                                       f"fp64 oracle fwd+bwd over full V and d), rate scaled to valid tokens/s"},
+            "step": f"forward + backward of the first {rows} of the batch's {nv} valid rows over full "
+                    f"V={x.workload.V} and d={x.workload.d} (a bounded sample; the whole batch would take "
+                    f"about {nv / value:.0f} s at this rate)",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "threads": threads, "kind": "oracle",
+                             "sample": f"each step: the first {rows} valid rows of the batch, plain C++ fp64 "
+                                       f"oracle forward + backward over full V and d on {threads} std::threads"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def run_cpu_table(args):
+    """The C++ oracle's rate on every workload, on this host's cores: the
+    small workloads (tiny, gpt1b, smallvocab) in full, the large ones
+    (llama8b, vocab256k) as the full-row LSE sweep every sampled parity check
+    needs plus a forward + backward of their first valid rows, with the
+    per-row rates and the whole-batch time extrapolated from them. One JSON
+    line per workload."""
+    from oracle import cpp_oracle
+    from synth_inputs import make_inputs
+    threads = cpp_oracle.default_threads()
+    names = args.cpu_table.split(",") if args.cpu_table != "all" else \
+        ["tiny", "gpt1b", "smallvocab", "llama8b", "vocab256k"]
+    for name in names:
+        x = make_inputs(name)
+        w = x.workload
+        nv = int((x.targets != -100).sum())
+        rec = {"cpu_table": name, "N": w.N, "d": w.d, "V": w.V, "n_valid": nv, "threads": threads,
+               "kind": "plain C++ fp64 oracle (std::thread)"}
+        if name in ("tiny", "gpt1b", "smallvocab"):
+            t0 = time.perf_counter()
+            cpp_oracle.forward_backward(x.H, x.W, x.targets, -100, threads=threads, bf16=x.bf16)
+            el = time.perf_counter() - t0
+            rec.update(what="forward + backward of the whole batch", seconds=el, valid_tokens_per_s=nv / el)
+        else:
+            t0 = time.perf_counter()
+            cpp_oracle.forward(x.H, x.W, x.targets, -100, threads=threads, bf16=x.bf16)
+            sweep = time.perf_counter() - t0
+            rows = 64
+            el = cpu_oracle_time(x, rows, threads)
+            rec.update(what="full-row LSE sweep (every valid row, forward only) + forward + backward of the "
+                            f"first {rows} valid rows",
+                       lse_sweep_seconds=sweep, lse_rows_per_s=nv / sweep,
+                       fwd_bwd_rows=rows, fwd_bwd_seconds=el, valid_tokens_per_s=rows / el,
+                       whole_batch_seconds_extrapolated=nv * el / rows)
+        print(json.dumps(rec), flush=True)
 
 
 def run_embedding(args):
@@ -363,7 +425,12 @@ def main():
                     help="skip the eager PyTorch context measurement (logits materialised)")
     ap.add_argument("--row-gather", action="store_true",
                     help="GEMMs read H's valid rows by TMA gather4 instead of a compacted copy")
+    ap.add_argument("--cpu-table", default="",
+                    help="time the C++ oracle per workload ('all' or a comma list) instead of the GPU path")
     args = ap.parse_args()
+    if args.cpu_table:
+        run_cpu_table(args)
+        return
     if args.impl == "reference":
         run_reference(args)
         return
@@ -525,10 +592,11 @@ def main():
     total_prof = sum(p["ms"] for p in phases.values())
     cpu = None
     if not args.no_cpu_baseline:
-        rate, el, rows, cores = cpu_oracle_rate(x, args.cpu_budget)
-        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"first {rows} valid rows of the batch, fp64 oracle forward+backward over full "
-                         f"V={w.V} and d={w.d} ({el:.1f} s), scaled to valid tokens/s"}
+        rate, el, rows, threads = cpu_oracle_rate(x, args.cpu_budget)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "threads": threads, "kind": "oracle",
+               "sample": f"first {rows} valid rows of the batch, plain C++ fp64 oracle forward + backward over "
+                         f"full V={w.V} and d={w.d} on {threads} std::threads ({el:.1f} s), "
+                         f"as valid tokens/s"}
     clocks = clk.summary()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -184,30 +184,6 @@ def profile_end() -> dict:
     return {name: {"ms": ms[i], "launches": int(cnt[i])} for i, name in enumerate(_abi.PHASE_NAMES)}
 
 
-class _LinearCrossEntropy(torch.autograd.Function):
-    """Training use: the forward call already produces dH and dW (the logits are
-    recomputed inside it, never stored); backward scales them by the incoming
-    scalar gradient."""
-
-    @staticmethod
-    def forward(ctx, H, W, targets, ignore_index):
-        loss, dH, dW = lce_forward_backward(H.contiguous(), W.contiguous(), targets.contiguous(), ignore_index)
-        ctx.save_for_backward(dH, dW)
-        ctx.w_dtype = W.dtype
-        return loss
-
-    @staticmethod
-    def backward(ctx, g):
-        dH, dW = ctx.saved_tensors
-        gH = dH if ctx.needs_input_grad[0] else None
-        gW = dW if ctx.needs_input_grad[1] else None
-        if gH is not None:
-            gH = (gH.float() * g).to(dH.dtype)
-        if gW is not None:
-            gW = (gW * g).to(ctx.w_dtype)
-        return gH, gW, None, None
-
-
 class _LinearCrossEntropySplit(torch.autograd.Function):
     """Two-call form: the forward computes the loss and keeps only the per-row
     lse [N]; the backward recomputes the logits and applies the incoming
@@ -229,18 +205,14 @@ class _LinearCrossEntropySplit(torch.autograd.Function):
                 dW.to(W.dtype) if ctx.needs_input_grad[1] else None, None, None)
 
 
-def linear_cross_entropy(H, W, targets, ignore_index: int = -100, fused: bool = False):
+def linear_cross_entropy(H, W, targets, ignore_index: int = -100):
     """loss = cross_entropy(H @ W^T, targets, ignore_index) without materialising logits.
 
-    fused=False (default) keeps only the per-row lse [N] from forward and runs
-    the gradient passes in backward, the incoming gradient applied inside the
-    kernels; the only elementwise step outside them is the cast of the fp32 dW
-    to a bf16 W's dtype that autograd requires. fused=True computes dH and dW
-    during the forward call and holds them until backward (dW is V x d fp32),
-    then scales them by the incoming gradient with one elementwise pass each;
-    it saves the backward's second compaction (about 0.6% of a step)."""
-    if fused:
-        return _LinearCrossEntropy.apply(H, W, targets, ignore_index)
+    The forward keeps only the per-row lse [N]; the backward recomputes the
+    logits and runs the gradient passes with the incoming gradient applied
+    inside the kernels (a device scalar read in the G epilogue, no host sync).
+    The only step outside the library is the cast of the fp32 dW to a bf16 W's
+    dtype that autograd requires."""
     return _LinearCrossEntropySplit.apply(H, W, targets, ignore_index)
 
 

@@ -1,10 +1,12 @@
 """Parity on the five workloads at full size, in the launch configuration the
 benchmark times (lce_run with a caller workspace):
-  tiny        fp32 inputs (tf32 tensor-core path), full oracle
+  tiny        fp32 inputs (split bf16 hi/lo products), full C++ oracle
   gpt1b       full oracle (every row, every gradient entry)
   smallvocab  full oracle
-  llama8b     full loss and every row's lse; dH on 256 seeded token rows and
-              dW on 256 seeded vocab rows
+  llama8b     full loss and every row's lse; dH on 256 seeded valid token
+              rows (and 8 padded ones, which must be exactly zero) and dW on
+              256 seeded vocab rows: 128 drawn from the targets of the batch,
+              the 16 most frequent included, and 128 uniformly over V
   vocab256k   same sampling as llama8b
 Tolerances: |loss| <= 1e-3, relative Frobenius <= 5e-3 for dH and dW, per-row
 lse <= 1e-3 (diagnostic). fp32 inputs take the split-precision path (bf16
@@ -16,6 +18,7 @@ torch = pytest.importorskip("torch")
 
 import chunked_vocab_cross_gb300 as lce  # noqa: E402
 import oracle  # noqa: E402
+from oracle import cpp_oracle  # noqa: E402
 from lce_testutil import TOL_LOSS, TOL_LSE, TOL_REL, np64, rel_fro, to_device  # noqa: E402
 from synth_inputs import IGNORE_INDEX, make_inputs  # noqa: E402
 
@@ -61,32 +64,57 @@ def test_full_oracle(name):
     assert errs["dH"] <= TOL_REL and errs["dW"] <= TOL_REL, errs
 
 
+def sample_rows(targets, V, seed=1234, n_tok=256, n_vocab=256, n_pad=8, n_head=16):
+    """Seeded samples for the large workloads: `n_tok` token rows drawn from the
+    valid positions (plus `n_pad` padded ones, whose dH must be exactly zero),
+    and `n_vocab` vocab rows, half of them drawn from the targets that occur in
+    the batch (always including the `n_head` most frequent, where the -onehot
+    term collects the most contributions) and half uniformly over V."""
+    rng = np.random.default_rng(seed)
+    valid = np.nonzero(targets != IGNORE_INDEX)[0]
+    padded = np.nonzero(targets == IGNORE_INDEX)[0]
+    rows = rng.choice(valid, min(n_tok, valid.size), replace=False)
+    if padded.size:
+        rows = np.concatenate([rows, rng.choice(padded, min(n_pad, padded.size), replace=False)])
+    ids, counts = np.unique(targets[valid], return_counts=True)
+    head = ids[np.argsort(-counts, kind="stable")[:n_head]]
+    rest = np.setdiff1d(ids, head)
+    tgt = np.concatenate([head, rng.choice(rest, min(n_vocab // 2 - head.size, rest.size), replace=False)])
+    others = np.setdiff1d(np.arange(V), tgt)
+    vocab = np.concatenate([tgt, rng.choice(others, n_vocab - tgt.size, replace=False)])
+    return np.sort(rows), np.sort(vocab)
+
+
 @pytest.mark.parametrize("name", ["llama8b", "vocab256k"])
 def test_sampled_oracle(name):
     x = make_inputs(name)
     g = _gpu_run(x)
-    rng = np.random.default_rng(1234)
-    rows = np.sort(rng.choice(x.workload.N, 256, replace=False))
-    vocab = np.sort(rng.choice(x.workload.V, 256, replace=False))
+    rows, vocab = sample_rows(x.targets, x.workload.V)
+    valid = x.targets != IGNORE_INDEX
+    in_batch = np.isin(vocab, x.targets[valid])
+    assert valid[rows].sum() >= 256 and in_batch.sum() >= 128
     # exact float64 copies of the inputs, made once (the oracle widens per block otherwise)
     ref = oracle.sampled_reference(x.H_f32().astype(np.float64), x.W_f32().astype(np.float64), x.targets,
                                    IGNORE_INDEX, rows, vocab)
-    valid = x.targets != IGNORE_INDEX
     dH_rows = np64(g["dH"][torch.from_numpy(rows).cuda()])
     dW_rows = np64(g["dW"][torch.from_numpy(vocab).cuda()])
     errs = {"loss": abs(g["loss"] - ref["loss"]),
             "lse": float(np.max(np.abs(g["lse"][valid] - ref["lse"]))),
-            "dH_rows": rel_fro(dH_rows, ref["dH_rows"]), "dW_rows": rel_fro(dW_rows, ref["dW_rows"])}
+            "dH_rows": rel_fro(dH_rows, ref["dH_rows"]), "dW_rows": rel_fro(dW_rows, ref["dW_rows"]),
+            "dW_target_rows": rel_fro(dW_rows[in_batch], ref["dW_rows"][in_batch]),
+            "dW_other_rows": rel_fro(dW_rows[~in_batch], ref["dW_rows"][~in_batch]),
+            "valid_token_rows": int(valid[rows].sum()), "target_vocab_rows": int(in_batch.sum())}
     print(name, errs)
     assert np.all(dH_rows[~valid[rows]] == 0.0)
     assert errs["loss"] <= TOL_LOSS and errs["lse"] <= TOL_LSE, errs
     assert errs["dH_rows"] <= TOL_REL and errs["dW_rows"] <= TOL_REL, errs
+    assert errs["dW_target_rows"] <= TOL_REL and errs["dW_other_rows"] <= TOL_REL, errs
 
 
 def test_tiny_fp32_split_path():
     x = make_inputs("tiny")
     g = _gpu_run(x)
-    ref = oracle.forward_backward(x.H.astype(np.float64), x.W.astype(np.float64), x.targets, IGNORE_INDEX)
+    ref = cpp_oracle.forward_backward(x.H, x.W, x.targets, IGNORE_INDEX)
     valid = x.targets != IGNORE_INDEX
     errs = {"loss": abs(g["loss"] - ref["loss"]),
             "lse": float(np.max(np.abs(g["lse"][valid] - ref["lse"]))),
