@@ -6,6 +6,7 @@ library has not been built: there is no CPU fallback.
 """
 from ._abi import LIB_PATH, LceError, lib  # noqa: F401
 from .ops import (  # noqa: F401
-    FusedOptimizer, device_status, embedding, embedding_backward, embedding_forward, launch_count, lce_backward, lce_compact, lce_forward, lce_forward_backward, lce_run, linear_cross_entropy,
+    FusedOptimizer, device_status, embedding, embedding_backward, embedding_forward, embedding_workspace_size,
+    launch_count, lce_backward, lce_compact, lce_forward, lce_forward_backward, lce_run, linear_cross_entropy,
     profile_begin, profile_end, workspace_size,
 )

@@ -823,7 +823,7 @@ lce_status_t lce_compact(const int64_t *targets, int64_t N, int64_t ignore_index
 
 namespace {
 struct EmbLayout {
-    size_t kA, vA, kB, vB, seg, pstart, pseg, pslot, mseg, mslot, mnp, counts, finals, partial, total;
+    size_t kA, vA, kB, vB, hist, counts, partial, total;
 };
 EmbLayout emb_layout(int64_t N, int64_t d) {
     EmbLayout L{};
@@ -833,21 +833,13 @@ EmbLayout emb_layout(int64_t N, int64_t d) {
         o += up256(bytes);
         return at;
     };
-    const size_t pmax = static_cast<size_t>(emb_pieces_max(N));
     L.kA = take(N * 4);
     L.vA = take(N * 4);
     L.kB = take(N * 4);
     L.vB = take(N * 4);
-    L.seg = take((N + 1) * 4);
-    L.pstart = take(pmax * 4);
-    L.pseg = take(pmax * 4);
-    L.pslot = take(pmax * 4);
-    L.mseg = take(N * 4);
-    L.mslot = take(N * 4);
-    L.mnp = take(N * 4);
+    L.hist = take(static_cast<size_t>(kEmbBuckets) * kEmbMaxSortBlocks * 4);
     L.counts = take(16);
-    L.finals = take(2 * sizeof(int *));
-    L.partial = take(static_cast<size_t>(emb_slots_max(N)) * d * 4);
+    L.partial = take(static_cast<size_t>(2 * emb_chunks_max(N)) * d * 4);
     L.total = o;
     return L;
 }
@@ -917,40 +909,52 @@ lce_status_t lce_embedding_backward(lce_dtype_t dtype, const void *dE, const int
     }
     uint8_t *base = static_cast<uint8_t *>(ws.p);
     auto ip = [&](size_t off) { return reinterpret_cast<int *>(base + off); };
-    EmbGroups g;
-    g.counts = ip(L.counts);
-    g.keys = reinterpret_cast<int **>(base + L.finals);
-    g.order = g.keys + 1;
-    g.seg = ip(L.seg);
-    g.piece_start = ip(L.pstart);
-    g.piece_seg = ip(L.pseg);
-    g.piece_slot = ip(L.pslot);
-    g.multi_seg = ip(L.mseg);
-    g.multi_slot = ip(L.mslot);
-    g.multi_np = ip(L.mnp);
+    int *counts = ip(L.counts);
+    int *hist = ip(L.hist);
     float *partial = reinterpret_cast<float *>(base + L.partial);
     if (!accumulate) {
         const size_t n = static_cast<size_t>(V) * d;
         k_zero_f32<<<4 * di->sms, 256, 0, st>>>(dW, n);
         LCE_CHECK_LAUNCH();
     }
-    k_emb_sort<<<1, kEmbSortThreads, 0, st>>>(tokens, static_cast<int>(N), pad_id, V, ip(L.kA), ip(L.vA), ip(L.kB),
-                                               ip(L.vB), g);
-    LCE_CHECK_LAUNCH();
+    // group the valid positions by token: stable LSD radix passes, ping-pong
+    // between the A and B key/position arrays (pass 0 reads the token ids)
+    const int sblocks = emb_sort_blocks(N);
+    const int span = static_cast<int>(emb_sort_span(N));
+    const int passes = emb_radix_passes(V);
+    int *keys[2] = {ip(L.kA), ip(L.kB)};
+    int *vals[2] = {ip(L.vA), ip(L.vB)};
+    for (int p = 0; p < passes; ++p) {
+        EmbSortIn in{};
+        in.t = tokens;
+        in.keys = p ? keys[(p - 1) & 1] : nullptr;
+        in.vals = p ? vals[(p - 1) & 1] : nullptr;
+        in.pad_id = pad_id;
+        in.V = V;
+        in.first = p == 0;
+        in.n = static_cast<int>(N);
+        const int shift = p * kEmbRadixBits;
+        k_emb_hist<<<sblocks, kEmbSortThreads, 0, st>>>(in, counts, span, shift, hist);
+        LCE_CHECK_LAUNCH();
+        k_emb_scatter<<<sblocks, kEmbSortThreads, 0, st>>>(in, counts, span, shift, hist, keys[p & 1], vals[p & 1]);
+        LCE_CHECK_LAUNCH();
+    }
+    const int *skeys = keys[(passes - 1) & 1];
+    const int *order = vals[(passes - 1) & 1];
     const unsigned slices = static_cast<unsigned>((d + kEmbSegCols - 1) / kEmbSegCols);
-    const int64_t pmax = emb_pieces_max(N);
-    const dim3 pgrid(static_cast<unsigned>(pmax < 8 * di->sms ? pmax : 8 * di->sms), slices);
+    const int64_t cmax = emb_chunks_max(N);
+    const dim3 pgrid(static_cast<unsigned>(cmax < 8 * di->sms ? cmax : 8 * di->sms), slices);
     if (dtype == LCE_BF16)
-        k_emb_pieces<__nv_bfloat16><<<pgrid, kEmbSegCols / 4, 0, st>>>(static_cast<const __nv_bfloat16 *>(dE), g,
-                                                                       static_cast<int>(d), dW, partial,
+        k_emb_segsum<__nv_bfloat16><<<pgrid, kEmbSegCols / 4, 0, st>>>(static_cast<const __nv_bfloat16 *>(dE), counts,
+                                                                       skeys, order, static_cast<int>(d), dW, partial,
                                                                        accumulate ? 1 : 0);
     else
-        k_emb_pieces<float><<<pgrid, kEmbSegCols / 4, 0, st>>>(static_cast<const float *>(dE), g, static_cast<int>(d),
-                                                               dW, partial, accumulate ? 1 : 0);
+        k_emb_segsum<float><<<pgrid, kEmbSegCols / 4, 0, st>>>(static_cast<const float *>(dE), counts, skeys, order,
+                                                               static_cast<int>(d), dW, partial, accumulate ? 1 : 0);
     LCE_CHECK_LAUNCH();
-    const int64_t mmax = N / kEmbPiece + 1;
-    const dim3 cgrid(static_cast<unsigned>(mmax < 4 * di->sms ? mmax : 4 * di->sms), slices);
-    k_emb_combine<<<cgrid, kEmbSegCols / 4, 0, st>>>(g, static_cast<int>(d), dW, partial, accumulate ? 1 : 0);
+    const dim3 cgrid(static_cast<unsigned>(cmax < 4 * di->sms ? cmax : 4 * di->sms), slices);
+    k_emb_combine<<<cgrid, kEmbSegCols / 4, 0, st>>>(counts, skeys, static_cast<int>(d), dW, partial,
+                                                    accumulate ? 1 : 0);
     LCE_CHECK_LAUNCH();
     return LCE_OK;
 }

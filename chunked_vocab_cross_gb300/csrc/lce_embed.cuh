@@ -5,21 +5,24 @@
 //             (the valid mask and the lookup in one kernel, no host sync:
 //             "为什么26万词表会卡死16GB显卡", section 2.3 稀疏索引引擎)
 //   backward  dW[v, :] (+)= sum of dE[i, :] over positions i with t_i == v,
-//             each sum taken in ascending position order (the batch's
-//             gradient rows aggregated per token after backward, same page,
-//             section 2.2; here in a fixed order instead of atomics, so the
-//             result is reproducible bit for bit)
+//             each sum taken in a fixed order (the batch's gradient rows
+//             aggregated per token after backward, same page, section 2.2;
+//             here without atomics, so the result is reproducible bit for bit)
 //
-// The backward groups the valid positions by token with one CTA: compaction
-// into (token, position) pairs, then a stable LSD radix sort on the token
-// (8-bit digits; within a 1024-element chunk an element's rank among equal
-// digits comes from a warp match plus per-warp digit offsets, chunks in
-// order), then the list of segment heads (first position of each token).
-// Segments are cut into pieces of at most kEmbPiece rows (fixed boundaries,
-// so the result does not depend on scheduling). A second kernel sums each
-// piece's rows in order, a block per (piece, 256-column slice): a segment of
-// one piece goes straight into dW, the pieces of a longer segment into fp32
-// partial rows, which a third kernel adds into dW in piece order.
+// The backward groups the valid positions by token with a stable LSD radix
+// sort spread over up to kEmbMaxSortBlocks CTAs: per pass (9-bit digits, as
+// many passes as the bits of V - 1 need), k_emb_hist counts each block's
+// digits and k_emb_scatter gives every block its offsets (column sums over
+// the blocks before it plus the digit totals before its digit) and places
+// its elements stably (within a 1024-element sub-chunk: a warp match gives
+// the rank among equal digits, per-warp digit counts give the warp's
+// offset; sub-chunks in order). The first pass reads the token ids directly
+// and drops padding and out-of-range ids, so no separate compaction runs.
+// The sorted list is then cut into fixed 32-element chunks: k_emb_segsum
+// sums, per chunk and 256-column slice, each run of equal tokens in order,
+// straight into dW when the run is the token's whole segment, else into the
+// run's partial row; k_emb_combine adds the partial rows of each segment that
+// spans chunks, in chunk order, into dW.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -29,29 +32,30 @@
 
 namespace lce {
 
-constexpr int kEmbSortThreads = 1024;
-constexpr int kEmbRadixBits = 8;
+constexpr int kEmbSortThreads = 1024;   // threads per sort block: one element each per sub-chunk
+constexpr int kEmbRadixBits = 9;
 constexpr int kEmbBuckets = 1 << kEmbRadixBits;
+constexpr int kEmbMaxSortBlocks = 64;
 constexpr int kEmbSegCols = 256;   // columns per segment-sum block (64 threads x 4)
-constexpr int kEmbPiece = 64;      // rows per piece of a segment
+constexpr int kEmbChunk = 32;      // sorted elements per segment-sum chunk
 
-// Bound on the pieces of N positions and on the partial rows they need.
-__host__ __device__ inline int64_t emb_pieces_max(int64_t N) { return N + N / kEmbPiece + 1; }
-__host__ __device__ inline int64_t emb_slots_max(int64_t N) { return 2 * (N / kEmbPiece) + 2; }
-
-// Grouping output, in the workspace (filled by k_emb_sort).
-struct EmbGroups {
-    int *counts;       // [0] valid positions, [1] segments, [2] pieces, [3] multi-piece segments
-    int **keys;        // -> token of each sorted position
-    int **order;       // -> sorted positions
-    int *seg;          // [nseg + 1] first sorted index of each segment
-    int *piece_start;  // [npieces] first sorted index of the piece
-    int *piece_seg;    // [npieces] its segment
-    int *piece_slot;   // [npieces] partial row, or -1 (single-piece segment: straight into dW)
-    int *multi_seg;    // [nmulti] segments of more than one piece
-    int *multi_slot;   // [nmulti] their first partial row (pieces in order)
-    int *multi_np;     // [nmulti] their piece counts
-};
+// Sort geometry for N positions: blocks and the elements each block covers
+// (a multiple of the sub-chunk), and the partial rows the chunks may need.
+__host__ __device__ inline int emb_sort_blocks(int64_t N) {
+    const int64_t b = (N + kEmbSortThreads - 1) / kEmbSortThreads;
+    return static_cast<int>(b < kEmbMaxSortBlocks ? (b > 0 ? b : 1) : kEmbMaxSortBlocks);
+}
+__host__ __device__ inline int64_t emb_sort_span(int64_t N) {
+    const int64_t b = emb_sort_blocks(N);
+    const int64_t per = (N + b - 1) / b;
+    return (per + kEmbSortThreads - 1) / kEmbSortThreads * kEmbSortThreads;
+}
+__host__ __device__ inline int64_t emb_chunks_max(int64_t N) { return (N + kEmbChunk - 1) / kEmbChunk; }
+__host__ __device__ inline int emb_radix_passes(int64_t V) {
+    int bits = 1;
+    while (bits < 31 && (int64_t(1) << bits) < V) ++bits;
+    return (bits + kEmbRadixBits - 1) / kEmbRadixBits;
+}
 
 template <typename T>
 struct Vec4;   // four consecutive elements
@@ -92,11 +96,6 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-// Single CTA: valid positions grouped by token, ascending positions within a
-// token. Workspace arrays of N int32 each: keys/vals (ping-pong x2), seg
-// (N + 1). Out: counts[0] = number of valid positions, counts[1] = number of
-// segments; order = the sorted positions, skey = their tokens, seg[s] = first
-// index of segment s in order (seg[nseg] = count).
 // Block-wide exclusive scan of one int per thread (1024 threads); returns
 // the prefix of this thread and sets *total. Uses warp_incl[32].
 __device__ __forceinline__ int block_scan_1024(int x, int *warp_incl, int *total) {
@@ -125,243 +124,260 @@ __device__ __forceinline__ int block_scan_1024(int x, int *warp_incl, int *total
     return pre;
 }
 
+// One element of a sort pass: pass 0 reads position i of the token ids
+// (valid: not padding and inside [0, V)), later passes element i of the
+// previous pass's output.
+struct EmbSortIn {
+    const int64_t *t;    // pass 0: token ids [N]
+    const int *keys;     // later passes: sorted keys and positions
+    const int *vals;
+    int64_t pad_id, V;
+    int first;           // 1 on pass 0
+    int n;               // pass 0: N; later: read from counts[0]
+};
+__device__ __forceinline__ bool emb_elem(const EmbSortIn &in, int i, int &key, int &val, bool &bad) {
+    bad = false;
+    if (in.first) {
+        const int64_t tok = in.t[i];
+        if (tok == in.pad_id) return false;
+        if (tok < 0 || tok >= in.V) {
+            bad = true;
+            return false;
+        }
+        key = static_cast<int>(tok);
+        val = i;
+        return true;
+    }
+    key = in.keys[i];
+    val = in.vals[i];
+    return true;
+}
+
+// Per block: digit counts of its elements -> hist[digit * blocks + block].
 __global__ void __launch_bounds__(kEmbSortThreads)
-    k_emb_sort(const int64_t *__restrict__ t, int N, int64_t pad_id, int64_t V, int *kA, int *vA, int *kB, int *vB,
-               EmbGroups g) {
-    int *seg = g.seg;
-    int *counts = g.counts;
-    __shared__ int wcnt[32][kEmbBuckets];   // per-warp digit counts, then per-warp digit offsets
+    k_emb_hist(EmbSortIn in, const int *__restrict__ counts, int span, int shift, int *__restrict__ hist) {
+    __shared__ int cnt[kEmbBuckets];
+    __shared__ int bad_any;
+    const int tid = threadIdx.x;
+    for (int b = tid; b < kEmbBuckets; b += kEmbSortThreads) cnt[b] = 0;
+    if (tid == 0) bad_any = 0;
+    __syncthreads();
+    const int n = in.first ? in.n : counts[0];
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * span;
+    const int64_t r1 = r0 + span < n ? r0 + span : n;
+    bool bad_seen = false;
+    for (int64_t i = r0 + tid; i < r1; i += kEmbSortThreads) {
+        int key, val;
+        bool bad;
+        if (emb_elem(in, static_cast<int>(i), key, val, bad)) atomicAdd(&cnt[(key >> shift) & (kEmbBuckets - 1)], 1);
+        bad_seen |= bad;
+    }
+    if (bad_seen) bad_any = 1;
+    __syncthreads();
+    for (int b = tid; b < kEmbBuckets; b += kEmbSortThreads) hist[b * gridDim.x + blockIdx.x] = cnt[b];
+    if (tid == 0 && bad_any) atomicOr(&g_status, DEV_TARGET_RANGE);
+}
+
+// Per block: its offsets from the histograms, then a stable placement of its
+// elements (sub-chunks of 1024 in order). Block 0 of pass 0 writes the
+// number of valid positions to counts[0].
+__global__ void __launch_bounds__(kEmbSortThreads)
+    k_emb_scatter(EmbSortIn in, int *__restrict__ counts, int span, int shift, const int *__restrict__ hist,
+                  int *__restrict__ k_out, int *__restrict__ v_out) {
+    __shared__ uint16_t wcnt[32][kEmbBuckets];   // per-warp digit counts, then per-warp offsets
     __shared__ int base[kEmbBuckets];
     __shared__ int ctot[kEmbBuckets];
     __shared__ int warp_incl[32];
-    __shared__ int bad_total;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned lt = (1u << lane) - 1u;
-    if (tid == 0) bad_total = 0;
+    const int nb = gridDim.x, b = blockIdx.x;
 
-    // 1. compaction: (token, position) of the valid positions, ascending
-    int running = 0, bad = 0;
-    for (int b0 = 0; b0 < N; b0 += kEmbSortThreads) {
-        const int i = b0 + tid;
-        const int64_t tok = i < N ? t[i] : pad_id;
-        const bool valid = tok != pad_id && tok >= 0 && tok < V;
-        bad += (i < N && tok != pad_id && !valid) ? 1 : 0;
-        const unsigned m = __ballot_sync(0xffffffffu, valid);
-        if (lane == 0) warp_incl[warp] = __popc(m);
-        __syncthreads();
-        if (warp == 0) {
-            int v = warp_incl[lane];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int n = __shfl_up_sync(0xffffffffu, v, o);
-                if (lane >= o) v += n;
-            }
-            warp_incl[lane] = v;
+    // offsets: digit totals before this digit + this digit's count in earlier blocks
+    int before = 0, tot = 0;
+    if (tid < kEmbBuckets) {
+        const int *h = hist + tid * nb;
+        for (int j = 0; j < nb; ++j) {
+            const int c = h[j];
+            tot += c;
+            before += j < b ? c : 0;
         }
-        __syncthreads();
-        if (valid) {
-            const int pos = running + (warp ? warp_incl[warp - 1] : 0) + __popc(m & lt);
-            kA[pos] = static_cast<int>(tok);
-            vA[pos] = i;
-        }
-        running += warp_incl[31];
-        __syncthreads();
     }
-    if (bad) atomicAdd(&bad_total, bad);
-    const int nv = running;
-
-    // 2. stable LSD radix sort on the token
-    int bits = 1;
-    while (bits < 31 && (int64_t(1) << bits) < V) ++bits;
-    int *ks = kA, *vs = vA, *kd = kB, *vd = vB;
-    for (int shift = 0; shift < bits; shift += kEmbRadixBits) {
-        for (int b = tid; b < kEmbBuckets; b += kEmbSortThreads) base[b] = 0;
-        __syncthreads();
-        for (int i = tid; i < nv; i += kEmbSortThreads) atomicAdd(&base[(ks[i] >> shift) & (kEmbBuckets - 1)], 1);
-        __syncthreads();
-        if (warp == 0) {   // exclusive scan of the 256 bucket counts, 8 per lane
-            int c[kEmbBuckets / 32], sum = 0;
-#pragma unroll
-            for (int j = 0; j < kEmbBuckets / 32; ++j) {
-                c[j] = base[lane * (kEmbBuckets / 32) + j];
-                sum += c[j];
-            }
-            int incl = sum;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int n = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += n;
-            }
-            int run = incl - sum;
-#pragma unroll
-            for (int j = 0; j < kEmbBuckets / 32; ++j) {
-                base[lane * (kEmbBuckets / 32) + j] = run;
-                run += c[j];
-            }
-        }
-        __syncthreads();
-        for (int b0 = 0; b0 < nv; b0 += kEmbSortThreads) {
-            for (int j = tid; j < 32 * kEmbBuckets; j += kEmbSortThreads) (&wcnt[0][0])[j] = 0;
-            __syncthreads();
-            const int i = b0 + tid;
-            const bool in = i < nv;
-            const int key = in ? ks[i] : 0;
-            const int val = in ? vs[i] : 0;
-            const int dg = in ? (key >> shift) & (kEmbBuckets - 1) : -1;
-            const unsigned peers = __match_any_sync(0xffffffffu, dg);
-            const int rank = __popc(peers & lt);
-            if (in && rank == 0) wcnt[warp][dg] = __popc(peers);
-            __syncthreads();
-            for (int b = tid; b < kEmbBuckets; b += kEmbSortThreads) {   // exclusive prefix over warps
-                int run = 0;
-                for (int w = 0; w < 32; ++w) {
-                    const int c = wcnt[w][b];
-                    wcnt[w][b] = run;
-                    run += c;
-                }
-                ctot[b] = run;
-            }
-            __syncthreads();
-            if (in) {
-                const int dst = base[dg] + wcnt[warp][dg] + rank;
-                kd[dst] = key;
-                vd[dst] = val;
-            }
-            __syncthreads();
-            for (int b = tid; b < kEmbBuckets; b += kEmbSortThreads) base[b] += ctot[b];
-            __syncthreads();
-        }
-        int *tk = ks, *tv = vs;
-        ks = kd, vs = vd, kd = tk, vd = tv;
-    }
-
-    // 3. segment heads (first index of each token's run), ascending
-    int nseg = 0;
-    for (int b0 = 0; b0 < nv; b0 += kEmbSortThreads) {
-        const int i = b0 + tid;
-        const bool head = i < nv && (i == 0 || ks[i] != ks[i - 1]);
-        const unsigned m = __ballot_sync(0xffffffffu, head);
-        if (lane == 0) warp_incl[warp] = __popc(m);
-        __syncthreads();
-        if (warp == 0) {
-            int v = warp_incl[lane];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int n = __shfl_up_sync(0xffffffffu, v, o);
-                if (lane >= o) v += n;
-            }
-            warp_incl[lane] = v;
-        }
-        __syncthreads();
-        if (head) seg[nseg + (warp ? warp_incl[warp - 1] : 0) + __popc(m & lt)] = i;
-        nseg += warp_incl[31];
-        __syncthreads();
-    }
-    if (tid == 0) seg[nseg] = nv;
+    int all;
+    const int pre = block_scan_1024(tid < kEmbBuckets ? tot : 0, warp_incl, &all);
+    if (tid < kEmbBuckets) base[tid] = pre + before;
+    if (in.first && b == 0 && tid == 0) counts[0] = all;
     __syncthreads();
 
-    // 4. pieces of at most kEmbPiece rows; segments of several pieces get
-    //    consecutive partial rows and an entry in the multi-piece list
-    int npieces = 0, nslots = 0, nmulti = 0;
-    for (int b0 = 0; b0 < nseg; b0 += kEmbSortThreads) {
-        const int sidx = b0 + tid;
-        const int len = sidx < nseg ? seg[sidx + 1] - seg[sidx] : 0;
-        const int np = (len + kEmbPiece - 1) / kEmbPiece;
-        const int multi = np > 1 ? 1 : 0;
-        int tot_p, tot_s, tot_m;
-        const int poff = npieces + block_scan_1024(np, warp_incl, &tot_p);
-        const int soff = nslots + block_scan_1024(multi ? np : 0, warp_incl, &tot_s);
-        const int moff = nmulti + block_scan_1024(multi, warp_incl, &tot_m);
-        for (int k = 0; k < np; ++k) {
-            g.piece_start[poff + k] = seg[sidx] + k * kEmbPiece;
-            g.piece_seg[poff + k] = sidx;
-            g.piece_slot[poff + k] = multi ? soff + k : -1;
+    const int n = in.first ? in.n : counts[0];
+    const int64_t r0 = static_cast<int64_t>(b) * span;
+    const int64_t r1 = r0 + span < n ? r0 + span : n;
+    for (int64_t c0 = r0; c0 < r1; c0 += kEmbSortThreads) {
+        for (int j = tid; j < 32 * kEmbBuckets / 2; j += kEmbSortThreads) reinterpret_cast<uint32_t *>(&wcnt[0][0])[j] = 0;
+        __syncthreads();
+        const int64_t i = c0 + tid;
+        int key = 0, val = 0;
+        bool bad = false;
+        const bool live = i < r1 && emb_elem(in, static_cast<int>(i), key, val, bad);
+        const int dg = live ? (key >> shift) & (kEmbBuckets - 1) : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, dg);
+        const int rank = __popc(peers & lt);
+        if (live && rank == 0) wcnt[warp][dg] = static_cast<uint16_t>(__popc(peers));
+        __syncthreads();
+        if (tid < kEmbBuckets) {   // exclusive prefix over warps
+            int run = 0;
+            for (int w = 0; w < 32; ++w) {
+                const int c = wcnt[w][tid];
+                wcnt[w][tid] = static_cast<uint16_t>(run);
+                run += c;
+            }
+            ctot[tid] = run;
         }
-        if (multi) {
-            g.multi_seg[moff] = sidx;
-            g.multi_slot[moff] = soff;
-            g.multi_np[moff] = np;
+        __syncthreads();
+        if (live) {
+            const int dst = base[dg] + wcnt[warp][dg] + rank;
+            k_out[dst] = key;
+            v_out[dst] = val;
         }
-        npieces += tot_p;
-        nslots += tot_s;
-        nmulti += tot_m;
-    }
-    if (tid == 0) {
-        counts[0] = nv;
-        counts[1] = nseg;
-        counts[2] = npieces;
-        counts[3] = nmulti;
-        g.keys[0] = ks;
-        g.order[0] = vs;
-        if (bad_total) atomicOr(&g_status, DEV_TARGET_RANGE);
+        __syncthreads();
+        if (tid < kEmbBuckets) base[tid] += ctot[tid];
+        __syncthreads();
     }
 }
 
-// Sum of one piece's rows in order, four columns per thread, sixteen rows
-// in flight: into dW (single-piece segment; added to dW's value when
-// accumulating) or into the piece's partial row. A block per (piece,
-// 256-column slice).
-constexpr int kEmbRowsInFlight = 16;
+// Run of equal keys containing sorted index j within [lo, hi): its first index.
+__device__ __forceinline__ int emb_run_start(const int *keys, int j, int lo) {
+    const int key = keys[j];
+    while (j > lo && keys[j - 1] == key) --j;
+    return j;
+}
+
+// Per (32-element chunk, 256-column slice): the sum of each run of equal
+// tokens in order, four columns per thread. The chunk's rows are loaded
+// eight at a time whatever the run boundaries (short runs are the common
+// case), together with dW's current value for every run that starts among
+// them (when accumulating), so that a batch costs one round trip to memory.
+// A run that is its token's whole segment goes into dW; the first / last run
+// of the chunk, when its segment continues into the chunk before / after,
+// into partial row 2c / 2c + 1.
+constexpr int kEmbRowsInFlight = 8;
+__device__ __forceinline__ void emb_flush(const int *keys, int nv, int c, int j0, int j1, int r0, int r1, int key,
+                                          const float *acc, float4 wcur, int d, int col, float *dW, float *partial,
+                                          int accumulate) {
+    const bool before = r0 == j0 && j0 > 0 && keys[j0 - 1] == key;
+    const bool after = r1 == j1 && j1 < nv && keys[j1] == key;
+    float4 v = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    float *out;
+    if (!before && !after) {
+        out = dW + static_cast<int64_t>(key) * d + col;
+        if (accumulate) v.x += wcur.x, v.y += wcur.y, v.z += wcur.z, v.w += wcur.w;
+    } else {
+        out = partial + static_cast<int64_t>(2 * c + (r0 == j0 ? 0 : 1)) * d + col;
+    }
+    *reinterpret_cast<float4 *>(out) = v;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(64, 8)
-    k_emb_pieces(const T *__restrict__ dE, EmbGroups g, int d, float *__restrict__ dW, float *__restrict__ partial,
+    k_emb_segsum(const T *__restrict__ dE, const int *__restrict__ counts, const int *__restrict__ keys,
+                 const int *__restrict__ order, int d, float *__restrict__ dW, float *__restrict__ partial,
                  int accumulate) {
-    const int npieces = g.counts[2];
-    const int *keys = g.keys[0];
-    const int *order = g.order[0];
+    const int nv = counts[0];
+    const int nchunks = (nv + kEmbChunk - 1) / kEmbChunk;
     const int col = blockIdx.y * kEmbSegCols + threadIdx.x * 4;
     if (col >= d) return;
-    for (int p = blockIdx.x; p < npieces; p += gridDim.x) {
-        const int sidx = g.piece_seg[p];
-        const int j0 = g.piece_start[p];
-        const int send = g.seg[sidx + 1];
-        const int j1 = j0 + kEmbPiece < send ? j0 + kEmbPiece : send;
-        const int slot = g.piece_slot[p];
-        float *out = slot < 0 ? dW + static_cast<int64_t>(keys[j0]) * d + col : partial + static_cast<int64_t>(slot) * d + col;
+    const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = blockIdx.x; c < nchunks; c += gridDim.x) {
+        const int j0 = c * kEmbChunk;
+        const int j1 = j0 + kEmbChunk < nv ? j0 + kEmbChunk : nv;
+        int key = -1, r0 = j0;
+        float4 wcur = zero4;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        if (slot < 0 && accumulate) {
-            const float4 a = *reinterpret_cast<const float4 *>(out);
-            acc[0] = a.x, acc[1] = a.y, acc[2] = a.z, acc[3] = a.w;
-        }
-        int j = j0;
-        for (; j + kEmbRowsInFlight <= j1; j += kEmbRowsInFlight) {
+        for (int jb = j0; jb < j1; jb += kEmbRowsInFlight) {
             float x[kEmbRowsInFlight][4];
+            int kk[kEmbRowsInFlight];
+            float4 pre[kEmbRowsInFlight];
 #pragma unroll
-            for (int r = 0; r < kEmbRowsInFlight; ++r)
-                Vec4<T>::load(dE + static_cast<int64_t>(order[j + r]) * d + col, x[r]);
+            for (int r = 0; r < kEmbRowsInFlight; ++r) kk[r] = jb + r < j1 ? keys[jb + r] : -1;
 #pragma unroll
-            for (int r = 0; r < kEmbRowsInFlight; ++r)
+            for (int r = 0; r < kEmbRowsInFlight; ++r) {
+                const int j = jb + r;
+                const bool starts = j < j1 && kk[r] != (r ? kk[r - 1] : key);
+                pre[r] = (accumulate && starts) ? *reinterpret_cast<const float4 *>(dW + static_cast<int64_t>(kk[r]) * d + col)
+                                                : zero4;
+                if (j < j1) {
+                    Vec4<T>::load(dE + static_cast<int64_t>(order[j]) * d + col, x[r]);
+                } else {
+                    x[r][0] = x[r][1] = x[r][2] = x[r][3] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < kEmbRowsInFlight; ++r) {
+                const int j = jb + r;
+                if (j >= j1) break;
+                if (kk[r] != key) {   // a run starts here; the one before (if any) is complete
+                    if (j > j0) emb_flush(keys, nv, c, j0, j1, r0, j, key, acc, wcur, d, col, dW, partial, accumulate);
+                    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+                    r0 = j;
+                    key = kk[r];
+                    wcur = pre[r];
+                }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) acc[k] += x[r][k];
+            }
         }
-        for (; j < j1; ++j) {
-            float x[4];
-            Vec4<T>::load(dE + static_cast<int64_t>(order[j]) * d + col, x);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) acc[k] += x[k];
-        }
-        *reinterpret_cast<float4 *>(out) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        emb_flush(keys, nv, c, j0, j1, r0, j1, key, acc, wcur, d, col, dW, partial, accumulate);
     }
 }
 
-// dW[v] (+)= the partial rows of a multi-piece segment, in piece order.
+// Segments that span chunks: the chunk holding a segment's first run adds
+// that run's partial row and the following chunks' partial rows of the
+// segment, in chunk order, into dW[token]. The block's 64 threads test 64
+// chunk boundaries at once to find how far the segment reaches, then each
+// thread loads its columns of those partial rows with eight loads in flight.
 __global__ void __launch_bounds__(64, 8)
-    k_emb_combine(EmbGroups g, int d, float *__restrict__ dW, const float *__restrict__ partial, int accumulate) {
-    const int nmulti = g.counts[3];
-    const int *keys = g.keys[0];
+    k_emb_combine(const int *__restrict__ counts, const int *__restrict__ keys, int d, float *__restrict__ dW,
+                  const float *__restrict__ partial, int accumulate) {
+    const int nv = counts[0];
+    const int nchunks = (nv + kEmbChunk - 1) / kEmbChunk;
     const int col = blockIdx.y * kEmbSegCols + threadIdx.x * 4;
-    if (col >= d) return;
-    for (int m = blockIdx.x; m < nmulti; m += gridDim.x) {
-        float *out = dW + static_cast<int64_t>(keys[g.seg[g.multi_seg[m]]]) * d + col;
+    const bool active = col < d;   // every thread takes part in the block-wide counts below
+    for (int c = blockIdx.x; c < nchunks; c += gridDim.x) {
+        const int j0 = c * kEmbChunk;
+        const int j1 = j0 + kEmbChunk < nv ? j0 + kEmbChunk : nv;
+        const int key = keys[j1 - 1];
+        if (!(j1 < nv && keys[j1] == key)) continue;           // the last run ends in this chunk (uniform)
+        const int rs = emb_run_start(keys, j1 - 1, j0);
+        if (rs == j0 && j0 > 0 && keys[j0 - 1] == key) continue;   // not the segment's first chunk (uniform)
+        // chunks c+1 .. c+len hold the rest of the segment
+        int len = 0;
+        for (;;) {
+            const int64_t e = static_cast<int64_t>(c + len + 1 + threadIdx.x) * kEmbChunk;
+            const bool in_seg = e < nv && keys[e] == key;
+            const int n = __syncthreads_count(in_seg);
+            len += n;
+            if (n < static_cast<int>(blockDim.x)) break;
+        }
+        if (!active) continue;
+        float *out = dW + static_cast<int64_t>(key) * d + col;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         if (accumulate) {
             const float4 a = *reinterpret_cast<const float4 *>(out);
             acc[0] = a.x, acc[1] = a.y, acc[2] = a.z, acc[3] = a.w;
         }
-        const float *src = partial + static_cast<int64_t>(g.multi_slot[m]) * d + col;
-        for (int k = 0; k < g.multi_np[m]; ++k) {
-            const float4 a = *reinterpret_cast<const float4 *>(src + static_cast<int64_t>(k) * d);
-            acc[0] += a.x, acc[1] += a.y, acc[2] += a.z, acc[3] += a.w;
+        // partial rows in chunk order: the first chunk's last run, then each
+        // following chunk's first run
+        for (int q0 = 0; q0 <= len; q0 += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int qq = q0 + q;
+                const int slot = qq == 0 ? 2 * c + (rs == j0 ? 0 : 1) : 2 * (c + qq);
+                v[q] = qq <= len ? *reinterpret_cast<const float4 *>(partial + static_cast<int64_t>(slot) * d + col)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (q0 + q <= len) acc[0] += v[q].x, acc[1] += v[q].y, acc[2] += v[q].z, acc[3] += v[q].w;
         }
         *reinterpret_cast<float4 *>(out) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     }

@@ -277,25 +277,36 @@ class FusedOptimizer:
         return loss, dH
 
 
-def embedding_forward(W, tokens, pad_id: int = 0, *, stream=None):
+def embedding_forward(W, tokens, pad_id: int = 0, *, out=None, stream=None):
     """E [N, d] (W's dtype): rows of W for the tokens, zero rows where the token
     is pad_id; non-padding ids outside [0, V) give zero rows and set the
-    target-range bit of the device status word."""
+    target-range bit of the device status word. `out` receives E if given."""
     if not (W.is_cuda and tokens.is_cuda) or W.dtype not in _DT or tokens.dtype != torch.int64:
         raise ValueError("W must be a bf16/fp32 CUDA tensor and tokens int64 on the same device")
     if W.dim() != 2 or tokens.dim() != 1 or not W.is_contiguous():
         raise ValueError("W must be a contiguous [V, d] tensor and tokens [N]")
     tokens = tokens.contiguous()
-    E = torch.empty((tokens.shape[0], W.shape[1]), dtype=W.dtype, device=W.device)
+    if out is None:
+        out = torch.empty((tokens.shape[0], W.shape[1]), dtype=W.dtype, device=W.device)
+    elif out.dtype != W.dtype or out.shape != (tokens.shape[0], W.shape[1]) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [N, d] tensor of W's dtype")
     _abi.check(_abi.lib().lce_embedding_forward(_DT[W.dtype], W.data_ptr(), tokens.data_ptr(), int(pad_id),
-                                                tokens.shape[0], W.shape[1], W.shape[0], E.data_ptr(),
+                                                tokens.shape[0], W.shape[1], W.shape[0], out.data_ptr(),
                                                 _stream(stream)), "lce_embedding_forward")
-    return E
+    return out
 
 
-def embedding_backward(dE, tokens, pad_id: int, V: int, *, dW=None, accumulate: bool = False, stream=None):
-    """dW [V, d] fp32 with each token's gradient rows summed in ascending
-    position order (overwritten, or added into a given dW with accumulate)."""
+def embedding_workspace_size(N: int, d: int) -> int:
+    """Bytes of scratch lce_embedding_backward needs for N positions of width d."""
+    return int(_abi.lib().lce_embedding_workspace_size(int(N), int(d)))
+
+
+def embedding_backward(dE, tokens, pad_id: int, V: int, *, dW=None, accumulate: bool = False, workspace=None,
+                       stream=None):
+    """dW [V, d] fp32 with each token's gradient rows summed in a fixed order
+    (overwritten, or added into a given dW with accumulate). `workspace`: a
+    uint8 CUDA tensor of at least embedding_workspace_size(N, d) bytes; without
+    it the library allocates its scratch on the stream."""
     if not (dE.is_cuda and tokens.is_cuda) or dE.dtype not in _DT or tokens.dtype != torch.int64:
         raise ValueError("dE must be a bf16/fp32 CUDA tensor and tokens int64 on the same device")
     if dE.dim() != 2 or tokens.dim() != 1 or dE.shape[0] != tokens.shape[0]:
@@ -306,9 +317,10 @@ def embedding_backward(dE, tokens, pad_id: int, V: int, *, dW=None, accumulate: 
         accumulate = False
     elif dW.dtype != torch.float32 or dW.shape != (V, dE.shape[1]) or not dW.is_contiguous():
         raise ValueError("dW must be a contiguous fp32 [V, d] tensor")
+    ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel()) if workspace is not None else (None, 0)
     _abi.check(_abi.lib().lce_embedding_backward(_DT[dE.dtype], dE.data_ptr(), tokens.data_ptr(), int(pad_id),
                                                  tokens.shape[0], dE.shape[1], V, dW.data_ptr(),
-                                                 1 if accumulate else 0, None, 0, _stream(stream)),
+                                                 1 if accumulate else 0, ws_ptr, ws_bytes, _stream(stream)),
                "lce_embedding_backward")
     return dW
 

@@ -306,8 +306,10 @@ lce_status_t lce_embedding_forward(lce_dtype_t dtype, const void *W, const int64
  * on the device and each row's sum is taken in ascending position order (the
  * batch's per-token gradients aggregated after backward, same page, section
  * 2.2, without atomics): results are reproducible bit for bit.
- * Long runs of one token are summed in fixed pieces of 64 positions, then the
- * pieces in order. Scratch: lce_embedding_workspace_size(N, d) bytes of
+ * The grouping is a stable radix sort of the valid positions by token over
+ * several CTAs; the sorted list is cut into fixed chunks of 32, each token's
+ * rows in a chunk are summed in order and a token whose rows span chunks
+ * gets its chunk sums added in chunk order. Scratch: lce_embedding_workspace_size(N, d) bytes of
  * `workspace` (device, 16-byte aligned), or NULL for a stream-ordered
  * allocation.
  */

@@ -177,8 +177,9 @@ def test_embedding_entry_points_host_checks_without_gpu(lib):
     ws = lib.lce_embedding_workspace_size(10, 64)
     assert ws > 0 and lib.lce_embedding_workspace_size(0, 64) == 0
     assert b(0, 4096, 4096, 0, 10, 64, 100, 4096, 0, 8192, ws - 1, None) == 6   # workspace too small
-    # scratch grows with N (grouping the positions) and N/64 partial rows of d, never with V
-    assert lib.lce_embedding_workspace_size(16384, 4096) < 16384 * 64 + 2 * (16384 // 64 + 1) * 4096 * 4
+    # scratch grows with N (grouping the positions) and two partial rows of d per
+    # 32 sorted positions, never with V
+    assert lib.lce_embedding_workspace_size(16384, 4096) < 16384 * 64 + 2 * (16384 // 32 + 1) * 4096 * 4
 
 
 def test_workspace_relations_across_options(lib):
