@@ -635,7 +635,11 @@ def main():
             and NCU_TRAFFIC["src_sha256"] == kernel_src_sha256() and not args.vocab_chunk and opt is None
             and not (args.row_gather or args.two_call or args.token_chunk)):
         traffic = NCU_TRAFFIC["bytes_per_launch"]
-    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    # The roofline is quoted against the burst bf16 peak (a 20-step timed
+    # region is well under a second of work); the sustained peak, measured
+    # over seconds under the power cap, is given beside it.
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     total_prof = sum(p["ms"] for p in phases.values())
     cpu = None
     if not args.no_cpu_baseline:
@@ -654,12 +658,12 @@ def main():
         "config": workload_desc(x, nv),
         "pct_dense_bf16_peak": {
             "useful_tflops": tflops_useful,
-            "of_burst": tflops_useful / float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
-            "of_sustained": tflops_useful / peak, "peaks": peak_src,
+            "of_burst": tflops_useful / peak,
+            "of_sustained": tflops_useful / peak_sus, "peaks": peak_src,
             "note": "useful FLOPs = 6*Nv*d*V; the path executes 8*Nv*d*V (logits recomputed in backward)"},
         "roofline": {"bound": "tensor", "kernel": f"k_gemm ({name})", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
-                     "peak_kind": f"bf16_tflops_sustained ({peak_src})",
+                     "peak_kind": f"bf16_tflops burst ({peak_src})", "frac_of_sustained": achieved / peak_sus,
                      "flops_per_launch": flops_launch, "ms_per_launch": per_launch_ms},
         "phases_ms_per_step": {k: v["ms"] / prof_steps for k, v in phases.items()},
         "phase_share": {k: (v["ms"] / total_prof if total_prof else None) for k, v in phases.items()},
