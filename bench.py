@@ -677,7 +677,7 @@ def main():
         "device_status": status,
         "clocks": clocks,
         "workspace_bytes": int(ws.numel()),
-        "vocab_chunk": args.vocab_chunk or "library default (6144)",
+        "vocab_chunk": args.vocab_chunk or "library default (6144-row chunks evened out over V)",
         "fused_optimizer": None if opt is None else f"{args.optim} on W in place (state fp32 [V,d]; no dW buffer)",
         "row_gather": bool(args.row_gather),
         "two_call": bool(args.two_call),

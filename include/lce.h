@@ -169,7 +169,7 @@ typedef struct {
     float *lse;               /* optional [N] fp32: per-row logsumexp (natural log), NaN on ignored rows */
     void *workspace;          /* optional device scratch; NULL = stream-ordered allocation */
     size_t workspace_bytes;   /* size of `workspace` */
-    int64_t vocab_chunk;      /* vocab rows per backward chunk; 0 = default (6144); else a multiple of 256 */
+    int64_t vocab_chunk;      /* vocab rows per backward chunk; 0 = default (6144-row chunks, evened out over V); else a multiple of 256 */
     lce_stream_t stream;
     const float *lse_in;      /* optional [N] fp32 per-row logsumexp from an earlier forward (the `lse`
                                  output of lce_run): the forward pass is skipped, only dH/dW are

@@ -201,7 +201,8 @@ def test_workspace_relations_across_options(lib):
         return lib.lce_workspace_size_args(ctypes.byref(a))
 
     n_pad = (5000 + 255) // 256 * 256
-    assert ws(optim=True) - ws() == n_pad * 6144 * 2                   # one more G buffer, default chunk
+    vc = 5632                                                           # V = 50000: 9 chunks of 5632
+    assert ws(optim=True) - ws() == n_pad * vc * 2                      # one more G buffer, default chunk
     assert ws(optim=True, vocab_chunk=2048) - ws(vocab_chunk=2048) == n_pad * 2048 * 2
     capped = ws(N=100000, token_chunk=4096)
     assert abs(capped - ws(N=200000, token_chunk=4096)) < 4096         # only the per-chunk loss sums grow
