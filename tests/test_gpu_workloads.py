@@ -9,7 +9,9 @@ benchmark times (lce_run with a caller workspace):
               the 16 most frequent included, and 128 uniformly over V
   vocab256k   same sampling as llama8b
 Tolerances: |loss| <= 1e-3, relative Frobenius <= 5e-3 for dH and dW, per-row
-lse <= 1e-3 (diagnostic). fp32 inputs take the split-precision path (bf16
+lse <= 1e-3 (diagnostic). Every workload also checks, on all output rows,
+that padded rows of dH are exactly zero and that the rows of dW sum to zero
+within the bound the bf16 rounding of G allows. fp32 inputs take the split-precision path (bf16
 hi/lo pairs, relative error about 2^-16) and meet the same bounds with room."""
 import numpy as np
 import pytest
@@ -35,6 +37,23 @@ def _gpu():
     yield
 
 
+def _full_size_properties(H, t, dH, dW):
+    """Properties that hold at any size, checked on every output row.
+    Padded rows of dH are exactly zero. Every row of G sums to zero, so the
+    rows of dW sum to zero: sum_v dW[v,:] = sum_i s_i H_i with s_i the row
+    sum of the bf16-rounded G, |s_i| <= 2^-9 * sum_v |g_iv| <= 2^-8 / Nv
+    (bf16 unit roundoff 2^-9; the lse error, below 1e-3 here, adds at most
+    1e-3 / Nv), hence |sum_v dW[v,:]|_2 <= (2^-8 + 1e-3) * mean_i |H_i|_2."""
+    valid = t != IGNORE_INDEX
+    assert torch.count_nonzero(dH[~valid]).item() == 0
+    col = dW.double().sum(0)
+    bound = (2.0 ** -8 + 1e-3) * H[valid].double().norm(dim=1).mean().item()
+    got = col.norm().item()
+    print("sum_v dW[v,:] norm", got, "bound", bound)
+    assert got <= bound, (got, bound)
+    return got, bound
+
+
 def _gpu_run(x):
     H, W, t = to_device(x)
     w = x.workload
@@ -42,6 +61,7 @@ def _gpu_run(x):
     loss, dH, dW, lse = lce.lce_forward_backward(H, W, t, IGNORE_INDEX, workspace=ws, return_lse=True)
     torch.cuda.synchronize()
     assert lce.device_status() == 0
+    _full_size_properties(H, t, dH, dW)
     out = {"loss": loss.item(), "lse": np64(lse), "dH": dH, "dW": dW}
     del H, W, ws
     return out
