@@ -233,8 +233,10 @@ struct Sched {
 // re-read per vocab tile stay in L2, at the cost of one pass over W per
 // group: for 39 row blocks of d = 4096 (78 MB) this cut the LSE launch's
 // DRAM reads by two thirds (3.2 -> 1.1 GB for a 24576-row vocab slice) and
-// the step by 4%; 69 MB of row blocks (d = 2048) gained nothing from it.
-constexpr long long kLseGroupBytes = 72LL << 20;
+// the step by 4%. A 48 MB budget (two groups for 29 row blocks of d = 4096,
+// 58 MB) is 1% faster per step than one group there; three groups (24 MB)
+// are slower again, and 69 MB of row blocks of d = 2048 gain nothing.
+constexpr long long kLseGroupBytes = 48LL << 20;
 __host__ __device__ inline int lse_group_rows(int m_blocks, int d, int nseg) {
     const long long block_bytes = static_cast<long long>(kPairM) * d * 2 * (nseg > 1 ? 2 : 1);
     long long r = kLseGroupBytes / block_bytes;
