@@ -73,6 +73,13 @@ def test_workspace_size_is_linear_in_N_not_N_times_V(lib):
     assert lib.lce_workspace_size(100, 4096, 100, 0, 300) == 0
 
 
+def test_default_vocab_chunk_is_evened_out_over_V(lib):
+    """The default backward chunk is 6144 rows spread evenly over the chunks V
+    needs (256-row tiles), visible in the G buffers of the workspace."""
+    for V, vc in ((32000, 5376), (50304, 5632), (128256, 6144), (262144, 6144), (1000, 1024), (6145, 3328)):
+        assert lib.lce_workspace_size(4096, 512, V, 0, 0) == lib.lce_workspace_size(4096, 512, V, 0, vc), V
+
+
 def test_args_struct_layout_matches_c():
     src = f"""
 #include <stdio.h>
