@@ -435,6 +435,8 @@ def main():
     ap.add_argument("--vocab-chunk", type=int, default=0, help="backward vocab chunk (0 = library default)")
     ap.add_argument("--optim", default="none", choices=["none", "sgd", "adamw"],
                     help="fuse an optimizer step on W into the backward (no dW buffer; W is updated every step)")
+    ap.add_argument("--optim-state", default="fp32", choices=["fp32", "bf16"],
+                    help="dtype of the fused optimizer's state (moments / momentum buffer)")
     ap.add_argument("--two-call", action="store_true",
                     help="forward (storing the per-row lse) and backward from the stored lse as two calls")
     ap.add_argument("--token-chunk", type=int, default=0,
@@ -493,7 +495,8 @@ def main():
                                         fused_optimizer=fused, row_gather=args.row_gather),
                      dtype=torch.uint8, device=dev)
     lse_buf = torch.empty(w.N, dtype=torch.float32, device=dev) if args.two_call else None
-    opt = lce.FusedOptimizer(W, args.optim, lr=1e-5) if fused else None
+    state_dtype = torch.bfloat16 if args.optim_state == "bf16" else torch.float32
+    opt = lce.FusedOptimizer(W, args.optim, lr=1e-5, state_dtype=state_dtype) if fused else None
 
     def run(Hx, tx, lx, dHx):
         kw = dict(workspace=ws, vocab_chunk=args.vocab_chunk, token_chunk=args.token_chunk,
@@ -678,7 +681,7 @@ def main():
         "clocks": clocks,
         "workspace_bytes": int(ws.numel()),
         "vocab_chunk": args.vocab_chunk or "library default (6144-row chunks evened out over V)",
-        "fused_optimizer": None if opt is None else f"{args.optim} on W in place (state fp32 [V,d]; no dW buffer)",
+        "fused_optimizer": None if opt is None else f"{args.optim} on W in place (state {args.optim_state} [V,d]; no dW buffer)",
         "row_gather": bool(args.row_gather),
         "two_call": bool(args.two_call),
         "token_chunk": args.token_chunk or None,

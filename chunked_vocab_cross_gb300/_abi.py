@@ -60,6 +60,7 @@ class LceOptim(ctypes.Structure):
         ("beta1", c_float), ("beta2", c_float), ("eps", c_float),
         ("step", c_int64),
         ("master_W", c_void_p), ("exp_avg", c_void_p), ("exp_avg_sq", c_void_p),
+        ("state_bf16", c_int),
     ]
 
 

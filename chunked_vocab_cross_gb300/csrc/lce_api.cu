@@ -541,8 +541,9 @@ lce_status_t run_rows(const lce_args_t *a, const DevInfo &di, uint8_t *base, con
         const lce_optim_t *o = a->optim;
         const bool use_m = o->kind == LCE_OPT_ADAMW || o->momentum != 0.f;
         const float *w32 = o->master_W ? o->master_W : (a->dtype == LCE_FP32 ? static_cast<const float *>(a->W) : nullptr);
-        if ((use_m && !encode_opt_map(&opt_maps[0], o->exp_avg, true, d, V)) ||
-            (o->kind == LCE_OPT_ADAMW && !encode_opt_map(&opt_maps[1], o->exp_avg_sq, true, d, V)) ||
+        const bool s32 = !o->state_bf16;
+        if ((use_m && !encode_opt_map(&opt_maps[0], o->exp_avg, s32, d, V)) ||
+            (o->kind == LCE_OPT_ADAMW && !encode_opt_map(&opt_maps[1], o->exp_avg_sq, s32, d, V)) ||
             (w32 && !encode_opt_map(&opt_maps[2], w32, true, d, V)) ||
             (a->dtype == LCE_BF16 && !encode_opt_map(&opt_maps[3], a->W, false, d, V)))
             return LCE_ERR_CUDA;
@@ -564,6 +565,7 @@ lce_status_t run_rows(const lce_args_t *a, const DevInfo &di, uint8_t *base, con
         oa.master = o->master_W;
         oa.m = o->exp_avg;
         oa.v = o->exp_avg_sq;
+        oa.s16 = o->state_bf16 ? 1 : 0;
     }
 
     const int n_chunks = static_cast<int>((a->V + Vc - 1) / Vc);
@@ -1117,6 +1119,6 @@ lce_status_t lce_selftest_wait_timeout(int64_t cycles, int32_t *gave_up, lce_str
     return LCE_OK;
 }
 
-int lce_version(void) { return 300; }
+int lce_version(void) { return 400; }
 
 }  // extern "C"

@@ -77,7 +77,8 @@ constexpr int kPairTx = 2 * kStageBytes;   // bytes both CTAs land on the even C
 // TMA swizzle pattern and stored to global memory by one bulk tensor store.
 constexpr int kEpiBufBytes = 4096;
 constexpr int kEpiBytes = 4 * 2 * kEpiBufBytes;
-constexpr int kGemmSmem = kStages * kStageBytes + kEpiBytes + 1024 /*alignment slack*/ + 256 /*barriers*/;
+constexpr int kBarrierBytes = 320;   // mbarriers, TMEM address slot and abort flag
+constexpr int kGemmSmem = kStages * kStageBytes + kEpiBytes + 1024 /*alignment slack*/ + kBarrierBytes;
 // The optimizer instantiation runs a 5-stage ring: the freed 32 KB doubles
 // each epilogue warp's staging area (16 KB), which holds the ring of W and
 // optimizer-state boxes the TMA engine streams through (the mainloop is as
@@ -85,9 +86,9 @@ constexpr int kGemmSmem = kStages * kStageBytes + kEpiBytes + 1024 /*alignment s
 template <int KIND>
 struct Cfg {
     static constexpr int kS = KIND == 2 /* KIND_BWD_OPT */ ? 5 : kStages;
-    static constexpr int kEpiWarp = (kGemmSmem - kS * kStageBytes - 1024 - 256) / 4;   // staging bytes per warp
+    static constexpr int kEpiWarp = (kGemmSmem - kS * kStageBytes - 1024 - kBarrierBytes) / 4;   // staging bytes per warp
 };
-constexpr int kOptLoadBars = 3;   // TMA load barriers per epilogue warp (optimizer ring)
+constexpr int kOptLoadBars = 5;   // TMA load barriers per epilogue warp (optimizer ring)
 constexpr long long kWaitCycles = 2000000000LL;   // ~1 s: far above any legitimate wait
 constexpr long long kDrainCycles = 200000000LL;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -179,7 +180,8 @@ struct OptArgs {
     void *W;               // [V][d] weights updated in place: bf16, or fp32 when w_fp32
     int w_fp32;
     float *master;         // optional fp32 [V][d] master copy of a bf16 W (W = its bf16 rounding)
-    float *m, *v;          // fp32 [V][d]: AdamW moments / SGD momentum buffer (m)
+    void *m, *v;           // [V][d]: AdamW moments / SGD momentum buffer (m), fp32 or bf16
+    int s16;               // m and v are bf16 (read, updated in fp32, stored rounded to nearest)
 };
 
 struct GemmArgs {
@@ -375,12 +377,20 @@ __device__ __forceinline__ void split_bf16(float x, float &hi, float &lo) {
 // Fused optimizer step on one 32-row x 16-column box of W held in a warp's
 // staging buffer, as the TMA engine loaded it: lane r updates row r from its
 // gradient g[0..15] (straight from TMEM). Buffer layout: first moment /
-// momentum buffer (fp32, 2 KB), second moment (fp32, 2 KB), then the weights:
-// fp32 (2 KB; the master copy or an fp32 W) or bf16 (1 KB); with a master
-// copy the bf16 rounding of W follows at 6 KB. fp32 rows of 64 bytes keep
-// 16-byte unit k of row r at unit k ^ ((r >> 1) & 3) (64-byte swizzle), bf16
-// rows of 32 bytes at unit k ^ ((r >> 2) & 1) (32-byte swizzle).
-constexpr int kOptM = 0, kOptV = 2048, kOptW = 4096, kOptWOut = 6144;
+// momentum buffer (fp32, 2 KB, or bf16 in its first 1 KB), second moment
+// (likewise), then the weights: fp32 (2 KB; the master copy or an fp32 W) or
+// bf16 (1 KB); with a master copy the bf16 rounding of W follows at 6 KB.
+// fp32 rows of 64 bytes keep 16-byte unit k of row r at unit k ^ ((r >> 1)
+// & 3) (64-byte swizzle), bf16 rows of 32 bytes at unit k ^ ((r >> 2) & 1)
+// (32-byte swizzle).
+// Byte offsets in one ring buffer: fp32 state {m 0, v 2048, weights 4096,
+// bf16 W out 6144}; bf16 state {m 0, v 1024, weights 2048, bf16 W out 4096}.
+struct OptLayout {
+    int m, v, w, wout;
+};
+__device__ __forceinline__ OptLayout opt_layout(const OptArgs &o) {
+    return o.s16 ? OptLayout{0, 1024, 2048, 4096} : OptLayout{0, 2048, 4096, 6144};
+}
 
 __device__ __forceinline__ float4 *opt_f32(uint8_t *buf, int off, int r, int k) {
     return reinterpret_cast<float4 *>(buf + off + r * 64 + ((k ^ ((r >> 1) & 3)) << 4));
@@ -389,29 +399,51 @@ __device__ __forceinline__ uint4 *opt_b16(uint8_t *buf, int off, int r, int k) {
     return reinterpret_cast<uint4 *>(buf + off + r * 32 + ((k ^ ((r >> 2) & 1)) << 4));
 }
 
+// eight bf16 (16 bytes) <-> eight floats
+__device__ __forceinline__ void unpack_bf16x8(uint4 x, float *f) {
+    const uint32_t u[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(u[i] << 16);
+        f[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ uint4 pack_bf16x8(const float *f) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                      pack_bf16x2(f[6], f[7]));
+}
+
 __device__ __forceinline__ void opt_row(const OptArgs &o, uint8_t *buf, int r, const float *g) {
     const bool use_m = o.kind == OPT_ADAMW || o.momentum != 0.f;
     const bool w32 = o.master || o.w_fp32;
+    const OptLayout L = opt_layout(o);
     float w[16], m[16], v[16];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         if (w32) {
-            const float4 x = *opt_f32(buf, kOptW, r, k);
+            const float4 x = *opt_f32(buf, L.w, r, k);
             w[4 * k] = x.x, w[4 * k + 1] = x.y, w[4 * k + 2] = x.z, w[4 * k + 3] = x.w;
         }
-        if (use_m) {
-            const float4 x = *opt_f32(buf, kOptM, r, k);
+        if (use_m && !o.s16) {
+            const float4 x = *opt_f32(buf, L.m, r, k);
             m[4 * k] = x.x, m[4 * k + 1] = x.y, m[4 * k + 2] = x.z, m[4 * k + 3] = x.w;
         }
-        if (o.kind == OPT_ADAMW) {
-            const float4 x = *opt_f32(buf, kOptV, r, k);
+        if (o.kind == OPT_ADAMW && !o.s16) {
+            const float4 x = *opt_f32(buf, L.v, r, k);
             v[4 * k] = x.x, v[4 * k + 1] = x.y, v[4 * k + 2] = x.z, v[4 * k + 3] = x.w;
+        }
+    }
+    if (o.s16) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            if (use_m) unpack_bf16x8(*opt_b16(buf, L.m, r, k), m + 8 * k);
+            if (o.kind == OPT_ADAMW) unpack_bf16x8(*opt_b16(buf, L.v, r, k), v + 8 * k);
         }
     }
     if (!w32) {
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-            const uint4 x = *opt_b16(buf, kOptW, r, k);
+            const uint4 x = *opt_b16(buf, L.w, r, k);
             const uint32_t u[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -438,13 +470,20 @@ __device__ __forceinline__ void opt_row(const OptArgs &o, uint8_t *buf, int r, c
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        if (use_m) *opt_f32(buf, kOptM, r, k) = make_float4(m[4 * k], m[4 * k + 1], m[4 * k + 2], m[4 * k + 3]);
-        if (o.kind == OPT_ADAMW)
-            *opt_f32(buf, kOptV, r, k) = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-        if (w32) *opt_f32(buf, kOptW, r, k) = make_float4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+        if (use_m && !o.s16) *opt_f32(buf, L.m, r, k) = make_float4(m[4 * k], m[4 * k + 1], m[4 * k + 2], m[4 * k + 3]);
+        if (o.kind == OPT_ADAMW && !o.s16)
+            *opt_f32(buf, L.v, r, k) = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        if (w32) *opt_f32(buf, L.w, r, k) = make_float4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+    }
+    if (o.s16) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            if (use_m) *opt_b16(buf, L.m, r, k) = pack_bf16x8(m + 8 * k);
+            if (o.kind == OPT_ADAMW) *opt_b16(buf, L.v, r, k) = pack_bf16x8(v + 8 * k);
+        }
     }
     if (!o.w_fp32) {
-        const int off = o.master ? kOptWOut : kOptW;
+        const int off = o.master ? L.wout : L.w;
 #pragma unroll
         for (int k = 0; k < 2; ++k)
             *opt_b16(buf, off, r, k) = make_uint4(pack_bf16x2(w[8 * k], w[8 * k + 1]), pack_bf16x2(w[8 * k + 2], w[8 * k + 3]),
@@ -472,12 +511,13 @@ __device__ __forceinline__ void opt_issue(const GemmMaps &maps, const OptArgs &o
     uint8_t *buf = q.base + b * q.bsz;
     uint64_t *bar = q.bar + b;
     mbar_arrive_expect_tx(bar, q.bytes);
-    if (o.kind == OPT_ADAMW || o.momentum != 0.f) tma_load_2d(buf + kOptM, &maps.opt_m, bar, col, row);
-    if (o.kind == OPT_ADAMW) tma_load_2d(buf + kOptV, &maps.opt_v, bar, col, row);
+    const OptLayout L = opt_layout(o);
+    if (o.kind == OPT_ADAMW || o.momentum != 0.f) tma_load_2d(buf + L.m, &maps.opt_m, bar, col, row);
+    if (o.kind == OPT_ADAMW) tma_load_2d(buf + L.v, &maps.opt_v, bar, col, row);
     if (o.master || o.w_fp32)
-        tma_load_2d(buf + kOptW, &maps.opt_w32, bar, col, row);
+        tma_load_2d(buf + L.w, &maps.opt_w32, bar, col, row);
     else
-        tma_load_2d(buf + kOptW, &maps.opt_w16, bar, col, row);
+        tma_load_2d(buf + L.w, &maps.opt_w16, bar, col, row);
     q.pend |= 1u << b;
 }
 
@@ -485,10 +525,11 @@ __device__ __forceinline__ void opt_issue(const GemmMaps &maps, const OptArgs &o
 __device__ __forceinline__ void opt_store(const GemmMaps &maps, const OptArgs &o, const OptRing &q, int p, int col,
                                           int row) {
     const uint8_t *buf = q.base + (p % q.nbuf) * q.bsz;
-    if (o.kind == OPT_ADAMW || o.momentum != 0.f) tma_store_2d(&maps.opt_m, buf + kOptM, col, row);
-    if (o.kind == OPT_ADAMW) tma_store_2d(&maps.opt_v, buf + kOptV, col, row);
-    if (o.master || o.w_fp32) tma_store_2d(&maps.opt_w32, buf + kOptW, col, row);
-    if (!o.w_fp32) tma_store_2d(&maps.opt_w16, buf + (o.master ? kOptWOut : kOptW), col, row);
+    const OptLayout L = opt_layout(o);
+    if (o.kind == OPT_ADAMW || o.momentum != 0.f) tma_store_2d(&maps.opt_m, buf + L.m, col, row);
+    if (o.kind == OPT_ADAMW) tma_store_2d(&maps.opt_v, buf + L.v, col, row);
+    if (o.master || o.w_fp32) tma_store_2d(&maps.opt_w32, buf + L.w, col, row);
+    if (!o.w_fp32) tma_store_2d(&maps.opt_w16, buf + (o.master ? L.wout : L.w), col, row);
     bulk_commit_group();
 }
 
@@ -750,17 +791,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;
         const int trow = quarter * 32 + lane;     // row within this CTA's 128 rows == TMEM lane
         uint8_t *stage_mine = epi_stage + (warp - 2) * EW;   // this warp's staging buffers
-        // fused optimizer: this warp's ring of W / state boxes in its staging
-        // area (three 5 KB buffers, or two 8 KB ones when fp32 weights move)
+        // fused optimizer: this warp's ring of W / state boxes in its 16 KB
+        // staging area: with fp32 state three 5 KB buffers, or two 8 KB ones
+        // when fp32 weights move; with bf16 state five 3 KB buffers (bf16 W),
+        // four of 4 KB (fp32 W) or three of 5 KB (fp32 master)
         OptRing ring{};
         if (KIND == KIND_BWD_OPT) {
             const bool w32 = a.opt.master || a.opt.w_fp32;
             ring.base = stage_mine;
             ring.bar = opt_bar + (warp - 2) * kOptLoadBars;
-            ring.nbuf = w32 ? 2 : 3;
-            ring.bsz = w32 ? 8192 : 5120;
-            ring.bytes = ((a.opt.kind == OPT_ADAMW || a.opt.momentum != 0.f) ? 2048u : 0u) +
-                         (a.opt.kind == OPT_ADAMW ? 2048u : 0u) + (w32 ? 2048u : 1024u);
+            // buffer bytes (1 KB multiples): the state boxes, the weights box and,
+            // with a master copy, the bf16 W box it is rounded into
+            ring.bsz = a.opt.s16 ? (w32 ? (a.opt.master ? 5120 : 4096) : 3072) : (w32 ? 8192 : 5120);
+            ring.nbuf = EW / ring.bsz < kOptLoadBars ? EW / ring.bsz : kOptLoadBars;
+            const uint32_t sb = a.opt.s16 ? 1024u : 2048u;   // one state box (16 columns x 32 rows)
+            ring.bytes = ((a.opt.kind == OPT_ADAMW || a.opt.momentum != 0.f) ? sb : 0u) +
+                         (a.opt.kind == OPT_ADAMW ? sb : 0u) + (w32 ? 2048u : 1024u);
         }
         int ebuf = 0;
         const float gscale = a.grad_ptr ? a.grad_scale * *a.grad_ptr : a.grad_scale;

@@ -220,27 +220,33 @@ class FusedOptimizer:
     """SGD or AdamW on the vocabulary matrix W, applied inside the backward
     pass of lce_run (the optimizer item of include/lce.h): each call of step()
     returns the loss and dH for the current W and leaves W updated, without a
-    gradient buffer for W ever existing. Holds the fp32 state (moments,
-    momentum buffer, optional fp32 master weights of a bf16 W) on W's device.
+    gradient buffer for W ever existing. Holds the state (moments or momentum
+    buffer, fp32 by default or bf16 with state_dtype=torch.bfloat16, as
+    torch.optim keeps them for a bf16 parameter; optional fp32 master weights
+    of a bf16 W) on W's device.
 
     The pages' training loop attaches an optimizer with algorithm "adamw" or
     "sgd" that updates weights in place during backward ("OjasX 0.6.1:
     Training a 1B-Parameter LLM in 6.35GB of RAM", usage listing)."""
 
     def __init__(self, W: torch.Tensor, algorithm: str = "adamw", lr: float = 3e-4, betas=(0.9, 0.999),
-                 eps: float = 1e-8, weight_decay: float = 0.0, momentum: float = 0.0, master_weights: bool = False):
+                 eps: float = 1e-8, weight_decay: float = 0.0, momentum: float = 0.0, master_weights: bool = False,
+                 state_dtype=torch.float32):
         if algorithm not in ("adamw", "sgd"):
             raise ValueError("algorithm must be 'adamw' or 'sgd'")
         if not W.is_cuda or not W.is_contiguous() or W.dtype not in _DT:
             raise ValueError("W must be a contiguous bf16 or fp32 CUDA tensor")
         if master_weights and W.dtype != torch.bfloat16:
             raise ValueError("master weights are kept for a bf16 W only")
+        if state_dtype not in (torch.float32, torch.bfloat16):
+            raise ValueError("state_dtype must be torch.float32 or torch.bfloat16")
+        self.state_dtype = state_dtype
         self.W = W
         self.algorithm = algorithm
         self.lr, self.betas, self.eps = float(lr), (float(betas[0]), float(betas[1])), float(eps)
         self.weight_decay, self.momentum = float(weight_decay), float(momentum)
         self.step_count = 0
-        z = lambda: torch.zeros(W.shape, dtype=torch.float32, device=W.device)  # noqa: E731
+        z = lambda: torch.zeros(W.shape, dtype=state_dtype, device=W.device)  # noqa: E731
         self.exp_avg = z() if (algorithm == "adamw" or momentum != 0.0) else None
         self.exp_avg_sq = z() if algorithm == "adamw" else None
         self.master = W.float() if master_weights else None
@@ -257,6 +263,7 @@ class FusedOptimizer:
         o.master_W = self.master.data_ptr() if self.master is not None else None
         o.exp_avg = self.exp_avg.data_ptr() if self.exp_avg is not None else None
         o.exp_avg_sq = self.exp_avg_sq.data_ptr() if self.exp_avg_sq is not None else None
+        o.state_bf16 = 1 if self.state_dtype == torch.bfloat16 else 0
         return o
 
     def step(self, H, targets, ignore_index: int = -100, *, grad_scale: float = 1.0, grad_loss=None,

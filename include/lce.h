@@ -135,7 +135,12 @@ lce_status_t lce_compact(const int64_t *targets, int64_t N, int64_t ignore_index
  * rewritten as its bf16 rounding. Every W row is updated exactly once per
  * call, after the last read of its old value (loss, lse and dH are those of
  * the old W). State arrays are fp32 [V,d], device, 16-byte aligned, owned by
- * the caller. Requirements (else LCE_ERR_ARG / LCE_ERR_NULL): dH given and
+ * the caller; with state_bf16 they are bf16 [V,d] instead, as torch.optim
+ * keeps them for a bf16 parameter: each is read, updated in fp32 (the update
+ * of w uses the fp32 values) and stored rounded to the nearest bf16, which
+ * halves their memory and traffic (12 instead of 20 bytes moved per W
+ * element for AdamW on a bf16 W). Requirements (else LCE_ERR_ARG /
+ * LCE_ERR_NULL): dH given and
  * dW NULL, accumulate_dW 0, one token chunk, step >= 1, lr >= 0,
  * weight_decay >= 0, 0 <= beta1, beta2 < 1, eps > 0, master_W only for bf16.
  */
@@ -148,8 +153,9 @@ typedef struct {
     float beta1, beta2, eps;  /* AdamW */
     int64_t step;             /* 1-based number of this update */
     float *master_W;          /* optional fp32 [V,d] master weights of a bf16 W */
-    float *exp_avg;           /* fp32 [V,d]: AdamW first moment, SGD momentum buffer */
-    float *exp_avg_sq;        /* fp32 [V,d]: AdamW second moment */
+    void *exp_avg;            /* [V,d] fp32 (bf16 with state_bf16): AdamW first moment, SGD momentum buffer */
+    void *exp_avg_sq;         /* [V,d] fp32 (bf16 with state_bf16): AdamW second moment */
+    int state_bf16;           /* nonzero: exp_avg / exp_avg_sq are bf16 */
 } lce_optim_t;
 
 /* Full argument set for lce_run. Zero-initialise, then fill. */

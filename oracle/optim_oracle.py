@@ -28,6 +28,12 @@ One step, elementwise, in float64 (w the weights, g their gradient, t the
             v  = beta2 * v + (1 - beta2) * g^2
             w  = w - lr * (m / (1 - beta1^t)) / (sqrt(v / (1 - beta2^t)) + eps)
 
+State kept in bf16 (state_bf16=True, the layout torch.optim uses for a bf16
+parameter): the step itself is the same; the state it returns is rounded to
+the nearest bf16 (ties to even), while the update of w uses the unrounded
+values, so w is the fp32-state step's w and the state is that step's state
+rounded.
+
 Pins (tests/test_oracle_pins.py): torch.optim.SGD and torch.optim.AdamW in
 float64 over several steps (independent implementations of the same rules),
 the closed form of AdamW's first step (m_hat = g and v_hat = g^2, so the step
@@ -43,13 +49,14 @@ __all__ = ["optimizer_step"]
 
 def optimizer_step(kind: str, w, g, *, lr: float, step: int, weight_decay: float = 0.0,
                    momentum: float = 0.0, beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8,
-                   exp_avg=None, exp_avg_sq=None) -> dict:
+                   exp_avg=None, exp_avg_sq=None, state_bf16: bool = False) -> dict:
     """One optimizer step on weights w with gradient g (any shapes, equal).
 
     Returns float64 arrays {"w", "exp_avg", "exp_avg_sq"} (state entries None
     when the rule keeps none); the inputs are not modified. exp_avg is the SGD
     momentum buffer or AdamW's first moment, exp_avg_sq AdamW's second moment;
-    None means zeros (the state before the first step)."""
+    None means zeros (the state before the first step). With state_bf16
+    the returned state is rounded to bf16 (as float64 values)."""
     if step < 1:
         raise ValueError("step is 1-based")
     w = np.array(w, dtype=np.float64)
@@ -66,12 +73,23 @@ def optimizer_step(kind: str, w, g, *, lr: float, step: int, weight_decay: float
             out_m = m
         else:
             out_m = None
-        return {"w": w - lr * d, "exp_avg": out_m, "exp_avg_sq": None}
+        return {"w": w - lr * d, "exp_avg": _store(out_m, state_bf16), "exp_avg_sq": None}
     if kind == "adamw":
         w = w * (1.0 - lr * weight_decay)
         m = beta1 * m + (1.0 - beta1) * g
         v = beta2 * v + (1.0 - beta2) * g * g
         m_hat = m / (1.0 - beta1 ** step)
         v_hat = v / (1.0 - beta2 ** step)
-        return {"w": w - lr * m_hat / (np.sqrt(v_hat) + eps), "exp_avg": m, "exp_avg_sq": v}
+        return {"w": w - lr * m_hat / (np.sqrt(v_hat) + eps), "exp_avg": _store(m, state_bf16),
+                "exp_avg_sq": _store(v, state_bf16)}
     raise ValueError(f"unknown optimizer {kind!r}")
+
+
+def _store(x, bf16: bool):
+    """State as stored: unchanged, or rounded to the nearest bf16 (ties to
+    even) by way of its float32 value."""
+    if x is None or not bf16:
+        return x
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    r = (u + (((u >> np.uint32(16)) & np.uint32(1)) + np.uint32(0x7FFF))) & np.uint32(0xFFFF0000)
+    return r.view(np.float32).astype(np.float64)

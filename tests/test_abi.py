@@ -61,7 +61,7 @@ def test_host_checks_without_gpu(lib):
     a.vocab_chunk, a.dH = 0, 4096
     assert lib.lce_run(ctypes.byref(a)) == 1           # dH without dW
     assert lib.lce_status_string(0) == b"ok"
-    assert lib.lce_version() == 300          # 0.3.0: optimizer, row gather, embedding entry points
+    assert lib.lce_version() == 400          # 0.4.0: bf16 optimizer state
 
 
 def test_workspace_size_is_linear_in_N_not_N_times_V(lib):
@@ -94,7 +94,7 @@ int main(void) {{
   printf(" %zu", sizeof(lce_optim_t));
 #define G(x) printf(" %zu", offsetof(lce_optim_t, x));
   G(kind) G(lr) G(weight_decay) G(momentum) G(beta1) G(beta2) G(eps) G(step) G(master_W) G(exp_avg)
-  G(exp_avg_sq)
+  G(exp_avg_sq) G(state_bf16)
   printf("\\n"); return 0; }}
 """
     with tempfile.TemporaryDirectory() as d:

@@ -296,3 +296,62 @@ def test_optimizer_state_layouts(case):
         w_or, m_or, v_or = o["w"], o["exp_avg"], o["exp_avg_sq"]
         if dt == "bf16" and not master:
             w_or = _bf16_round(w_or)   # W is stored as the bf16 rounding of the update (the contract)
+
+
+@pytest.mark.parametrize("kind,hp", [("adamw", dict(lr=1e-2, betas=(0.9, 0.99), weight_decay=0.1)),
+                                     ("sgd", dict(lr=0.05, momentum=0.9, weight_decay=0.01))])
+def test_bf16_state_first_step_equals_fp32_state_rounded(kind, hp):
+    """Optimizer state kept in bf16: on a first step (zero state, exact in
+    both) the update of W is bit for bit the fp32-state update (both run in
+    fp32 from the same values), and the stored state is the fp32 state
+    rounded to the nearest bf16, bit for bit."""
+    x = make_inputs("gpt1b", N=700, d=192, V=2500, padding=("random_frac", 0.2), seqs=1)
+    H, W0, t = to_device(x)
+    outs = {}
+    for sd in (torch.float32, torch.bfloat16):
+        W = W0.clone()
+        opt = lce.FusedOptimizer(W, kind, master_weights=True, state_dtype=sd, **hp)
+        assert opt.exp_avg.dtype == sd
+        opt.step(H, t, IGNORE_INDEX, vocab_chunk=1024)
+        torch.cuda.synchronize()
+        assert lce.device_status() == 0
+        outs[sd] = (W, opt.master, opt.exp_avg, opt.exp_avg_sq)
+    W32, M32, m32, v32 = outs[torch.float32]
+    W16, M16, m16, v16 = outs[torch.bfloat16]
+    assert torch.equal(W32, W16) and torch.equal(M32, M16)
+    assert torch.equal(m32.to(torch.bfloat16), m16)
+    if kind == "adamw":
+        assert torch.equal(v32.to(torch.bfloat16), v16)
+
+
+def test_adamw_bf16_state_three_steps_against_oracle():
+    """AdamW with bf16 moments on a bf16 W with fp32 master weights, three
+    steps, against the oracle's step with bf16-rounded state: the step within
+    the gradient's bound, the moments within it plus one bf16 rounding
+    (2^-8 relative)."""
+    x = make_inputs("gpt1b", N=1100, d=200, V=5000, padding=("random_frac", 0.3), seqs=1)
+    H0, W, t = to_device(x)
+    opt = lce.FusedOptimizer(W, "adamw", lr=1e-2, betas=(0.9, 0.99), weight_decay=0.1, master_weights=True,
+                             state_dtype=torch.bfloat16)
+    w_or = x.W_f32().astype(np.float64)
+    m_or = v_or = None
+    rng = np.random.default_rng(5)
+    for step in (1, 2, 3):
+        Hs = x.H_f32() if step == 1 else _bf16_round(rng.standard_normal(x.H_f32().shape))
+        Hd = H0 if step == 1 else torch.from_numpy(Hs.astype(np.float32)).to("cuda").to(torch.bfloat16)
+        ref = _oracle_grad(Hs, _bf16_round(w_or), x.targets)
+        eps = 10.0 * float(np.max(np.abs(ref["dW"])))          # step nearly linear in g
+        opt.eps = eps
+        master_old = np64(opt.master)
+        loss, dH = opt.step(Hd, t, IGNORE_INDEX, vocab_chunk=1024)
+        torch.cuda.synchronize()
+        assert lce.device_status() == 0
+        o = _step("adamw", w_or, ref["dW"], lr=1e-2, step=step, weight_decay=0.1, beta1=0.9, beta2=0.99, eps=eps,
+                  exp_avg=m_or, exp_avg_sq=v_or, state_bf16=True)
+        errs = {"loss": abs(loss.item() - ref["loss"]), "step": rel_fro(np64(opt.master) - master_old, o["w"] - w_or),
+                "m": rel_fro(np64(opt.exp_avg), o["exp_avg"]), "v": rel_fro(np64(opt.exp_avg_sq), o["exp_avg_sq"])}
+        print(step, errs)
+        assert errs["loss"] <= TOL_LOSS and errs["step"] <= TOL_REL, errs
+        assert errs["m"] <= TOL_REL + 2.0 ** -8 and errs["v"] <= 2 * TOL_REL + 2.0 ** -8, errs
+        assert torch.equal(W, opt.master.to(torch.bfloat16))
+        w_or, m_or, v_or = o["w"], o["exp_avg"], o["exp_avg_sq"]

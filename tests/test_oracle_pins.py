@@ -347,6 +347,30 @@ def test_adamw_first_step_closed_form():
     np.testing.assert_allclose(r["w"], w - 0.01 * g / (np.abs(g) + 1e-8), rtol=1e-14, atol=0)
 
 
+def test_bf16_state_rounding_matches_torch_and_leaves_w_unchanged():
+    """State kept in bf16: the returned state is the fp32-state step's state
+    rounded to the nearest bf16 as torch converts it, and w is the fp32-state
+    step's w (the update uses the unrounded values)."""
+    torch = pytest.importorskip("torch")
+    g = np.random.default_rng(21)
+    w0 = g.standard_normal((5, 7))
+    grads = g.standard_normal((5, 7)) * 0.3
+    for kind, hp in (("adamw", dict(lr=1e-2, beta1=0.9, beta2=0.99, eps=1e-6, weight_decay=0.1)),
+                     ("sgd", dict(lr=0.05, momentum=0.9, weight_decay=0.01))):
+        m0 = torch.tensor(g.standard_normal((5, 7))).to(torch.bfloat16).double().numpy()
+        v0 = torch.tensor(g.uniform(0.1, 1.0, (5, 7))).to(torch.bfloat16).double().numpy()
+        a = oracle.optimizer_step(kind, w0, grads, step=3, exp_avg=m0, exp_avg_sq=v0 if kind == "adamw" else None,
+                                  **hp)
+        b = oracle.optimizer_step(kind, w0, grads, step=3, exp_avg=m0, exp_avg_sq=v0 if kind == "adamw" else None,
+                                  state_bf16=True, **hp)
+        np.testing.assert_array_equal(a["w"], b["w"])
+        for k in ("exp_avg", "exp_avg_sq"):
+            if a[k] is None:
+                continue
+            ref = torch.tensor(a[k]).float().to(torch.bfloat16).double().numpy()
+            np.testing.assert_array_equal(b[k], ref)
+
+
 def test_zero_gradient_without_decay_only_decays_the_moments():
     g0 = np.zeros((3, 4))
     w = np.arange(12.0).reshape(3, 4)
