@@ -32,8 +32,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # from an ncu capture of a reduced-V case with the same per-launch tile
 # counts; valid only for the kernel sources it was captured from (sha256
 # prefix below) and the default vocab chunk, else reported null.
-NCU_TRAFFIC = {"workload": "llama8b", "kernel": "backward", "bytes_per_launch": 1251.9e6,
-               "src_sha256": "929f481b9eae8f0e"}
+NCU_TRAFFIC = {"workload": "llama8b", "kernel": "backward", "bytes_per_launch": 1259.2e6,
+               "src_sha256": "82eb0f5c70cd7b9f"}
 
 
 def kernel_src_sha256(texts=None) -> str:
