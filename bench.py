@@ -32,8 +32,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # from an ncu capture of a reduced-V case with the same per-launch tile
 # counts; valid only for the kernel sources it was captured from (sha256
 # prefix below) and the default vocab chunk, else reported null.
-NCU_TRAFFIC = {"workload": "llama8b", "kernel": "backward", "bytes_per_launch": 1259.2e6,
-               "src_sha256": "82eb0f5c70cd7b9f"}
+NCU_TRAFFIC = {"workload": "llama8b", "kernel": "backward", "bytes_per_launch": 1198.7e6,
+               "src_sha256": "11cb97543dbc797e"}
 
 
 def kernel_src_sha256(texts=None) -> str:
@@ -437,6 +437,8 @@ def main():
                     help="fuse an optimizer step on W into the backward (no dW buffer; W is updated every step)")
     ap.add_argument("--optim-state", default="fp32", choices=["fp32", "bf16"],
                     help="dtype of the fused optimizer's state (moments / momentum buffer)")
+    ap.add_argument("--dw-dtype", default="fp32", choices=["fp32", "bf16"],
+                    help="dtype of the dW output (bf16: each fp32 accumulator rounded once, half the dW bytes)")
     ap.add_argument("--two-call", action="store_true",
                     help="forward (storing the per-row lse) and backward from the stored lse as two calls")
     ap.add_argument("--token-chunk", type=int, default=0,
@@ -489,7 +491,8 @@ def main():
     loss = torch.empty((), dtype=torch.float32, device=dev)
     dH = torch.empty_like(H)
     fused = args.optim != "none"
-    dW = None if fused else torch.empty(W.shape, dtype=torch.float32, device=dev)
+    dw_dtype = torch.bfloat16 if args.dw_dtype == "bf16" else torch.float32
+    dW = None if fused else torch.empty(W.shape, dtype=dw_dtype, device=dev)
     ws = torch.empty(lce.workspace_size(w.N, w.d, w.V, dtype=W.dtype, vocab_chunk=args.vocab_chunk,
                                         token_chunk=args.token_chunk,
                                         fused_optimizer=fused, row_gather=args.row_gather),
@@ -583,7 +586,7 @@ def main():
         b = i % 2
         stream.wait_event(copied[b])
         H_e, t_e = bufs[b]
-        if opt is None and not (args.row_gather or args.two_call or args.token_chunk):
+        if opt is None and args.dw_dtype == "fp32" and not (args.row_gather or args.two_call or args.token_chunk):
             l, _, _ = lce.lce_forward_backward(H_e, W, t_e, -100, vocab_chunk=args.vocab_chunk, workspace=ws)
         else:
             l = torch.empty((), dtype=torch.float32, device=dev)
@@ -636,7 +639,7 @@ def main():
     traffic = None
     if (NCU_TRAFFIC["workload"] == w.name and NCU_TRAFFIC["kernel"] == name and w.V == 128256
             and NCU_TRAFFIC["src_sha256"] == kernel_src_sha256() and not args.vocab_chunk and opt is None
-            and not (args.row_gather or args.two_call or args.token_chunk)):
+            and args.dw_dtype == "fp32" and not (args.row_gather or args.two_call or args.token_chunk)):
         traffic = NCU_TRAFFIC["bytes_per_launch"]
     # The roofline is quoted against the burst bf16 peak (a 20-step timed
     # region is well under a second of work); the sustained peak, measured
@@ -682,6 +685,7 @@ def main():
         "workspace_bytes": int(ws.numel()),
         "vocab_chunk": args.vocab_chunk or "library default (6144-row chunks evened out over V)",
         "fused_optimizer": None if opt is None else f"{args.optim} on W in place (state {args.optim_state} [V,d]; no dW buffer)",
+        "dW_dtype": None if opt is not None else args.dw_dtype,
         "row_gather": bool(args.row_gather),
         "two_call": bool(args.two_call),
         "token_chunk": args.token_chunk or None,

@@ -81,6 +81,7 @@ class LceArgs(ctypes.Structure):
         ("token_chunk", c_int64),
         ("optim", c_void_p),
         ("row_gather", c_int),
+        ("dW_bf16", c_int),
     ]
 
 

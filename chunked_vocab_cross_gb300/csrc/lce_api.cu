@@ -322,6 +322,10 @@ lce_status_t check_args(const lce_args_t *a) {
         return LCE_ERR_SHAPE;
     if (a->d % 8) return LCE_ERR_ALIGN;   // bf16 rows (operands or their split copies) of 16-byte multiples
     if (a->row_gather && !row_gather_ok(a->dtype, a->d)) return LCE_ERR_ARG;
+    // a bf16 dW is written once per element: bf16 inputs, no accumulation, one token chunk
+    if (a->dW_bf16 && (!a->dW || a->dtype != LCE_BF16 || a->accumulate_dW ||
+                       (a->token_chunk > 0 && a->token_chunk < a->N)))
+        return LCE_ERR_ARG;
     auto mis = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
     if (mis(a->H) || mis(a->W) || (a->dH && mis(a->dH)) || (a->dW && mis(a->dW)) ||
         (a->workspace && mis(a->workspace)))
@@ -531,7 +535,8 @@ lce_status_t run_rows(const lce_args_t *a, const DevInfo &di, uint8_t *base, con
         if (!encode_store_map(&st_g[b][0], G + b * gbuf, false, Vc, L.N_pad) ||
             !encode_store_map(&st_g[b][1], G_lo + b * gbuf, false, Vc, L.N_pad))
             return LCE_ERR_CUDA;
-    if ((a->dW && !encode_store_map(&st_dw, a->dW, true, d, V)) || !encode_store_map(&st_dh, dHacc, true, d, L.N_pad))
+    if ((a->dW && !encode_store_map(&st_dw, a->dW, !a->dW_bf16, d, V)) ||
+        !encode_store_map(&st_dh, dHacc, true, d, L.N_pad))
         return LCE_ERR_CUDA;
 
     OptArgs oa{};
@@ -598,6 +603,7 @@ lce_status_t run_rows(const lce_args_t *a, const DevInfo &di, uint8_t *base, con
             }
             g.mn3d = 1 | (mn3d_d ? 6 : 0);
             g.dW = a->dW;
+            g.dw_bf16 = a->dW_bf16 ? 1 : 0;
             g.acc_dw = ctx.acc_dw ? 1 : 0;
             g.dH_acc = dHacc;
             g.acc_dh = j > 0 ? 1 : 0;
@@ -1119,6 +1125,6 @@ lce_status_t lce_selftest_wait_timeout(int64_t cycles, int32_t *gave_up, lce_str
     return LCE_OK;
 }
 
-int lce_version(void) { return 400; }
+int lce_version(void) { return 500; }
 
 }  // extern "C"

@@ -200,8 +200,9 @@ struct GemmArgs {
     // next chunk [v0n, v0n+vlenn) (if has_next)
     int v0, vlen, v0n, vlenn, has_cur, has_next, v0w, vlenw, has_dw;
     const float *lse2;     // per compacted row: lse / ln 2
-    float *dW;             // [V][d]
+    float *dW;             // [V][d] fp32, or bf16 when dw_bf16
     int acc_dw;            // add into dW instead of overwriting
+    int dw_bf16;           // dW is written as bf16 (each fp32 accumulator rounded to nearest)
     float *dH_acc;         // [rows][d] fp32
     int acc_dh;            // add into dHacc (every chunk after the first)
     float grad_scale;      // multiplies G
@@ -943,7 +944,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         uint8_t *sbuf = stage_mine + ebuf * kEpiBufBytes;
                         if (lane == 0) bulk_wait_group_read<1>();   // this buffer's store of two chunks ago has read it
                         __syncwarp();
-                        if (t.type == T_G) {
+                        if (t.type == T_G || (t.type == T_DW && a.dw_bf16)) {
                             // bf16 rows of 64 bytes; 16-byte unit k of row `lane` at unit k ^ ((lane >> 1) & 3)
                             float lo[32];
                             if (a.nseg > 1) {

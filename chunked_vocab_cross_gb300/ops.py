@@ -50,7 +50,8 @@ def lce_run(H, W, targets, ignore_index: int = -100, *, loss=None, dH=None, dW=N
             grad_scale: float = 1.0, lse=None, workspace=None, vocab_chunk: int = 0, lse_in=None, grad_loss=None,
             token_chunk: int = 0, optim=None, row_gather: bool = False, stream=None) -> None:
     """Raw lce_run over caller-provided output tensors. `optim` is an
-    _abi.LceOptim (a fused optimizer step on W) or None."""
+    _abi.LceOptim (a fused optimizer step on W) or None. dW may be fp32 or,
+    for bf16 inputs without accumulation, bf16."""
     _check_inputs(H, W, targets)
     a = _abi.LceArgs()
     a.dtype = _DT[H.dtype]
@@ -63,6 +64,7 @@ def lce_run(H, W, targets, ignore_index: int = -100, *, loss=None, dH=None, dW=N
     a.grad_loss = grad_loss.data_ptr() if grad_loss is not None else None
     a.dH = dH.data_ptr() if dH is not None else None
     a.dW = dW.data_ptr() if dW is not None else None
+    a.dW_bf16 = 1 if (dW is not None and dW.dtype == torch.bfloat16) else 0
     a.accumulate_dW = 1 if accumulate_dW else 0
     a.grad_scale = float(grad_scale)
     a.lse = lse.data_ptr() if lse is not None else None
@@ -94,18 +96,19 @@ def lce_forward(H, W, targets, ignore_index: int = -100, *, return_lse: bool = F
 def lce_forward_backward(H, W, targets, ignore_index: int = -100, *, dW=None, accumulate_dW: bool = False,
                          grad_scale: float = 1.0, vocab_chunk: int = 0, return_lse: bool = False,
                          workspace=None, token_chunk: int = 0, stream=None):
-    """Loss, dH (H's dtype, zero on ignored rows) and dW (fp32) in one pass."""
+    """Loss, dH (H's dtype, zero on ignored rows) and dW (fp32, or the given
+    dW's dtype: bf16 for bf16 inputs without accumulation) in one pass."""
     _check_inputs(H, W, targets)
     loss = torch.empty((), dtype=torch.float32, device=H.device)
     dH = torch.empty_like(H)
     if dW is None:
         dW = torch.empty(W.shape, dtype=torch.float32, device=W.device)
         accumulate_dW = False
-    elif dW.dtype != torch.float32 or dW.shape != W.shape or not dW.is_contiguous():
-        raise ValueError("dW must be a contiguous fp32 tensor shaped like W")
+    elif dW.dtype not in (torch.float32, torch.bfloat16) or dW.shape != W.shape or not dW.is_contiguous():
+        raise ValueError("dW must be a contiguous fp32 (or bf16) tensor shaped like W")
     lse = torch.empty(H.shape[0], dtype=torch.float32, device=H.device) if return_lse else None
-    simple = (H.dtype == torch.bfloat16 and not accumulate_dW and grad_scale == 1.0 and vocab_chunk == 0
-              and not return_lse and workspace is None and token_chunk == 0)
+    simple = (H.dtype == torch.bfloat16 and dW.dtype == torch.float32 and not accumulate_dW and grad_scale == 1.0
+              and vocab_chunk == 0 and not return_lse and workspace is None and token_chunk == 0)
     if simple:
         _abi.check(_abi.lib().lce_forward_backward(H.data_ptr(), W.data_ptr(), targets.data_ptr(),
                                                    int(ignore_index), H.shape[0], H.shape[1], W.shape[0],
@@ -133,7 +136,10 @@ def lce_backward(H, W, targets, lse, ignore_index: int = -100, *, grad_loss=None
     if dW is None:
         dW = torch.empty(W.shape, dtype=torch.float32, device=W.device)
         accumulate_dW = False
-    if (H.dtype == torch.bfloat16 and not accumulate_dW and vocab_chunk == 0 and workspace is None):
+    if dW.dtype not in (torch.float32, torch.bfloat16) or dW.shape != W.shape or not dW.is_contiguous():
+        raise ValueError("dW must be a contiguous fp32 (or bf16) tensor shaped like W")
+    if (H.dtype == torch.bfloat16 and dW.dtype == torch.float32 and not accumulate_dW and vocab_chunk == 0
+            and workspace is None):
         _abi.check(_abi.lib().lce_backward(H.data_ptr(), W.data_ptr(), targets.data_ptr(), int(ignore_index),
                                            H.shape[0], H.shape[1], W.shape[0], lse.data_ptr(),
                                            grad_loss.data_ptr() if grad_loss is not None else None,
@@ -200,9 +206,12 @@ class _LinearCrossEntropySplit(torch.autograd.Function):
     @staticmethod
     def backward(ctx, g):
         H, W, targets, lse = ctx.saved_tensors
-        dH, dW = lce_backward(H, W, targets, lse, ctx.ignore_index, grad_loss=g)
+        # the gradient of W in W's dtype, written by the library (a bf16 W
+        # gets a bf16 dW: each fp32 accumulator rounded once)
+        dW = torch.empty(W.shape, dtype=W.dtype, device=W.device)
+        dH, dW = lce_backward(H, W, targets, lse, ctx.ignore_index, grad_loss=g, dW=dW)
         return (dH if ctx.needs_input_grad[0] else None,
-                dW.to(W.dtype) if ctx.needs_input_grad[1] else None, None, None)
+                dW if ctx.needs_input_grad[1] else None, None, None)
 
 
 def linear_cross_entropy(H, W, targets, ignore_index: int = -100):
@@ -210,9 +219,8 @@ def linear_cross_entropy(H, W, targets, ignore_index: int = -100):
 
     The forward keeps only the per-row lse [N]; the backward recomputes the
     logits and runs the gradient passes with the incoming gradient applied
-    inside the kernels (a device scalar read in the G epilogue, no host sync).
-    The only step outside the library is the cast of the fp32 dW to a bf16 W's
-    dtype that autograd requires."""
+    inside the kernels (a device scalar read in the G epilogue, no host sync)
+    and dW written in W's dtype by the library."""
     return _LinearCrossEntropySplit.apply(H, W, targets, ignore_index)
 
 

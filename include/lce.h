@@ -194,6 +194,10 @@ typedef struct {
                                  bytes per pipeline stage against one tiled load). The dense index
                                  list of "为什么26万词表会卡死16GB显卡", section 2.3 稀疏索引引擎,
                                  used directly as the operand's row map. */
+    int dW_bf16;              /* nonzero: dW is bf16 [V,d] (the fp32 accumulator of each element
+                                 rounded to nearest once), for a bf16 W whose gradient is kept in
+                                 its own dtype; half the dW bytes. bf16 inputs only, not with
+                                 accumulate_dW or token chunks (else LCE_ERR_ARG). */
 } lce_args_t;
 
 /* Forward, or forward + backward when dH/dW are given, or backward alone

@@ -60,8 +60,15 @@ def test_host_checks_without_gpu(lib):
     assert lib.lce_run(ctypes.byref(a)) == 2           # chunk not a multiple of 256
     a.vocab_chunk, a.dH = 0, 4096
     assert lib.lce_run(ctypes.byref(a)) == 1           # dH without dW
+    a.dH, a.dW, a.dW_bf16 = 4096, 4096, 1
+    a.dtype = 1
+    assert lib.lce_run(ctypes.byref(a)) == 10          # bf16 dW of fp32 inputs
+    a.dtype, a.accumulate_dW = 0, 1
+    assert lib.lce_run(ctypes.byref(a)) == 10          # bf16 dW accumulated into
+    a.accumulate_dW, a.token_chunk = 0, 4
+    assert lib.lce_run(ctypes.byref(a)) == 10          # bf16 dW over token chunks
     assert lib.lce_status_string(0) == b"ok"
-    assert lib.lce_version() == 400          # 0.4.0: bf16 optimizer state
+    assert lib.lce_version() == 500          # 0.5.0: bf16 dW output
 
 
 def test_workspace_size_is_linear_in_N_not_N_times_V(lib):
@@ -90,7 +97,7 @@ int main(void) {{
 #define F(x) printf(" %zu", offsetof(lce_args_t, x));
   F(dtype) F(H) F(W) F(targets) F(ignore_index) F(N) F(d) F(V) F(loss) F(dH) F(dW)
   F(accumulate_dW) F(grad_scale) F(lse) F(workspace) F(workspace_bytes) F(vocab_chunk) F(stream)
-  F(lse_in) F(grad_loss) F(token_chunk) F(optim) F(row_gather)
+  F(lse_in) F(grad_loss) F(token_chunk) F(optim) F(row_gather) F(dW_bf16)
   printf(" %zu", sizeof(lce_optim_t));
 #define G(x) printf(" %zu", offsetof(lce_optim_t, x));
   G(kind) G(lr) G(weight_decay) G(momentum) G(beta1) G(beta2) G(eps) G(step) G(master_W) G(exp_avg)

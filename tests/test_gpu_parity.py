@@ -266,6 +266,55 @@ def test_autograd_split_form():
     assert abs(loss.item() - ref["loss"]) <= TOL_LOSS
     assert rel_fro(np64(H.grad), 3 * ref["dH"]) <= 1e-2
     assert rel_fro(np64(W.grad), 3 * ref["dW"]) <= 1e-2
+    assert W.grad.dtype == torch.bfloat16
+
+
+def test_autograd_bf16_W_grad_is_the_fp32_gradient_rounded_once():
+    """W.grad of a bf16 W is written in bf16 by the library: each element the
+    fp32 accumulator of the fp32-dW path rounded to nearest, bit for bit."""
+    x = make_inputs("gpt1b", N=300, d=128, V=2100, padding=("random_frac", 0.1), seqs=1)
+    H, W, t = to_device(x)
+    W.requires_grad_(True)
+    loss = lce.linear_cross_entropy(H, W, t, IGNORE_INDEX)
+    loss.backward()
+    _, lse = lce.lce_forward(H, W.detach(), t, IGNORE_INDEX, return_lse=True)
+    _, dW32 = lce.lce_backward(H, W.detach(), t, lse, IGNORE_INDEX, grad_loss=torch.ones((), device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.equal(W.grad.view(torch.int16), dW32.to(torch.bfloat16).view(torch.int16))
+
+
+@pytest.mark.parametrize("shape", [(1500, 512, 6000), (333, 72, 1000), (300, 64, 50257)],
+                         ids=["gpt1b_small", "d72_ragged", "V50257"])
+def test_bf16_dW_output_is_fp32_dW_rounded(shape):
+    """dW_bf16: the dW tiles are staged and stored as bf16; every element equals
+    the fp32 output rounded to nearest, loss and dH are bitwise those of the
+    fp32-dW call, and the result is within the bf16 tolerance of the oracle."""
+    N, d, V = shape
+    x = make_inputs("gpt1b", N=N, d=d, V=V, padding=("random_frac", 0.2), seqs=1)
+    H, W, t = to_device(x)
+    l32, dH32, dW32 = lce.lce_forward_backward(H, W, t, IGNORE_INDEX)
+    dW16 = torch.full(W.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    l16, dH16, dW16 = lce.lce_forward_backward(H, W, t, IGNORE_INDEX, dW=dW16)
+    torch.cuda.synchronize()
+    assert lce.device_status() == 0
+    assert dW16.dtype == torch.bfloat16
+    assert torch.equal(l16, l32) and torch.equal(dH16.view(torch.int16), dH32.view(torch.int16))
+    assert torch.equal(dW16.view(torch.int16), dW32.to(torch.bfloat16).view(torch.int16))
+    ref = oracle.forward_backward(x.H_f32(), x.W_f32(), x.targets, IGNORE_INDEX)
+    assert rel_fro(np64(dW16), ref["dW"]) <= TOL_REL
+
+
+def test_bf16_dW_refused_where_it_would_be_rounded_twice():
+    x = make_inputs("gpt1b", N=200, d=64, V=900, padding=("random_frac", 0.1), seqs=1)
+    H, W, t = to_device(x)
+    dW16 = torch.zeros(W.shape, dtype=torch.bfloat16, device="cuda")
+    for kw in (dict(accumulate_dW=True), dict(token_chunk=100)):
+        with pytest.raises(RuntimeError) as e:
+            lce.lce_forward_backward(H, W, t, IGNORE_INDEX, dW=dW16, **kw)
+        assert e.value.code == 10                     # LCE_ERR_ARG
+    with pytest.raises(RuntimeError) as e:
+        lce.lce_forward_backward(H.float(), W.float(), t, IGNORE_INDEX, dW=dW16)
+    assert e.value.code == 10
 
 
 # ---------------------------------------------------------- token chunk cap
