@@ -304,6 +304,29 @@ def test_bf16_dW_output_is_fp32_dW_rounded(shape):
     assert rel_fro(np64(dW16), ref["dW"]) <= TOL_REL
 
 
+@pytest.mark.parametrize("kw", [dict(row_gather=True), dict(vocab_chunk=768), dict(vocab_chunk=256, row_gather=True)],
+                         ids=["row_gather", "chunk768", "chunk256_gather"])
+def test_bf16_dW_output_with_other_options(kw):
+    """The bf16 dW output under row gather and other vocab chunks (a ragged
+    last chunk): still the fp32 output of the same options rounded once."""
+    x = make_inputs("gpt1b", N=700, d=256, V=2000, padding=("random_frac", 0.25), seqs=1)
+    H, W, t = to_device(x)
+    outs = []
+    for dt in (torch.float32, torch.bfloat16):
+        loss = torch.empty((), dtype=torch.float32, device="cuda")
+        dH = torch.empty_like(H)
+        dW = torch.full(W.shape, float("nan"), dtype=dt, device="cuda")
+        lce.lce_run(H, W, t, IGNORE_INDEX, loss=loss, dH=dH, dW=dW, **kw)
+        outs.append((loss, dH, dW))
+    torch.cuda.synchronize()
+    assert lce.device_status() == 0
+    (l32, dH32, dW32), (l16, dH16, dW16) = outs
+    assert torch.equal(l16, l32) and torch.equal(dH16.view(torch.int16), dH32.view(torch.int16))
+    assert torch.equal(dW16.view(torch.int16), dW32.to(torch.bfloat16).view(torch.int16))
+    ref = oracle.forward_backward(x.H_f32(), x.W_f32(), x.targets, IGNORE_INDEX)
+    assert rel_fro(np64(dW16), ref["dW"]) <= TOL_REL
+
+
 def test_bf16_dW_refused_where_it_would_be_rounded_twice():
     x = make_inputs("gpt1b", N=200, d=64, V=900, padding=("random_frac", 0.1), seqs=1)
     H, W, t = to_device(x)
