@@ -49,6 +49,8 @@ SIGNATURES = {
     "lce_embedding_workspace_size": (c_size_t, [c_int64, c_int64]),
     "lce_embedding_backward": (c_int, [c_int, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int64, c_void_p, c_int,
                                        c_void_p, c_size_t, c_void_p]),
+    "lce_embedding_backward_bf16": (c_int, [c_int, c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int64, c_void_p,
+                                            c_void_p, c_size_t, c_void_p]),
 }
 
 

@@ -33,6 +33,7 @@
 #include <atomic>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 #include <vector>
 
 #include "lce.h"
@@ -899,9 +900,12 @@ size_t lce_embedding_workspace_size(int64_t N, int64_t d) {
     return emb_layout(N, d).total;
 }
 
-lce_status_t lce_embedding_backward(lce_dtype_t dtype, const void *dE, const int64_t *tokens, int64_t pad_id,
-                                    int64_t N, int64_t d, int64_t V, float *dW, int accumulate, void *workspace,
-                                    size_t workspace_bytes, lce_stream_t stream) {
+namespace {
+// dW fp32 (accumulate allowed) or bf16 (dw_bf16: each row's fp32 sum rounded
+// once, overwritten)
+lce_status_t emb_backward(lce_dtype_t dtype, const void *dE, const int64_t *tokens, int64_t pad_id, int64_t N,
+                          int64_t d, int64_t V, void *dW, bool dw_bf16, int accumulate, void *workspace,
+                          size_t workspace_bytes, lce_stream_t stream) {
     lce_status_t s = check_emb(dtype, dE, dW, tokens, N, d, V);
     if (s != LCE_OK) return s;
     const EmbLayout L = emb_layout(N, d);
@@ -929,8 +933,10 @@ lce_status_t lce_embedding_backward(lce_dtype_t dtype, const void *dE, const int
     int *hist = ip(L.hist);
     float *partial = reinterpret_cast<float *>(base + L.partial);
     if (!accumulate) {
-        const size_t n = static_cast<size_t>(V) * d;
-        k_zero_f32<<<4 * di->sms, 256, 0, st>>>(dW, n);
+        // V*d fp32 elements, or the same bytes as half as many floats for bf16
+        // (d % 8 == 0: a multiple of four floats either way)
+        const size_t n = static_cast<size_t>(V) * d / (dw_bf16 ? 2 : 1);
+        k_zero_f32<<<4 * di->sms, 256, 0, st>>>(static_cast<float *>(dW), n);
         LCE_CHECK_LAUNCH();
     }
     // group the valid positions by token: stable LSD radix passes, ping-pong
@@ -960,19 +966,44 @@ lce_status_t lce_embedding_backward(lce_dtype_t dtype, const void *dE, const int
     const unsigned slices = static_cast<unsigned>((d + kEmbSegCols - 1) / kEmbSegCols);
     const int64_t cmax = emb_chunks_max(N);
     const dim3 pgrid(static_cast<unsigned>(cmax < 8 * di->sms ? cmax : 8 * di->sms), slices);
-    if (dtype == LCE_BF16)
-        k_emb_segsum<__nv_bfloat16><<<pgrid, kEmbSegCols / 4, 0, st>>>(static_cast<const __nv_bfloat16 *>(dE), counts,
-                                                                       skeys, order, static_cast<int>(d), dW, partial,
-                                                                       accumulate ? 1 : 0);
-    else
-        k_emb_segsum<float><<<pgrid, kEmbSegCols / 4, 0, st>>>(static_cast<const float *>(dE), counts, skeys, order,
-                                                               static_cast<int>(d), dW, partial, accumulate ? 1 : 0);
-    LCE_CHECK_LAUNCH();
+    const int acc = accumulate ? 1 : 0;
+    const int di32 = static_cast<int>(d);
+    auto segsum = [&](auto *out) {
+        using O = std::remove_pointer_t<decltype(out)>;
+        if (dtype == LCE_BF16)
+            k_emb_segsum<__nv_bfloat16, O><<<pgrid, kEmbSegCols / 4, 0, st>>>(
+                static_cast<const __nv_bfloat16 *>(dE), counts, skeys, order, di32, out, partial, acc);
+        else
+            k_emb_segsum<float, O><<<pgrid, kEmbSegCols / 4, 0, st>>>(static_cast<const float *>(dE), counts, skeys,
+                                                                      order, di32, out, partial, acc);
+    };
     const dim3 cgrid(static_cast<unsigned>(cmax < 4 * di->sms ? cmax : 4 * di->sms), slices);
-    k_emb_combine<<<cgrid, kEmbSegCols / 4, 0, st>>>(counts, skeys, static_cast<int>(d), dW, partial,
-                                                    accumulate ? 1 : 0);
+    if (dw_bf16) {
+        segsum(static_cast<__nv_bfloat16 *>(dW));
+        LCE_CHECK_LAUNCH();
+        k_emb_combine<__nv_bfloat16><<<cgrid, kEmbSegCols / 4, 0, st>>>(counts, skeys, di32,
+                                                                        static_cast<__nv_bfloat16 *>(dW), partial, 0);
+    } else {
+        segsum(static_cast<float *>(dW));
+        LCE_CHECK_LAUNCH();
+        k_emb_combine<float><<<cgrid, kEmbSegCols / 4, 0, st>>>(counts, skeys, di32, static_cast<float *>(dW), partial,
+                                                                acc);
+    }
     LCE_CHECK_LAUNCH();
     return LCE_OK;
+}
+}  // namespace
+
+lce_status_t lce_embedding_backward(lce_dtype_t dtype, const void *dE, const int64_t *tokens, int64_t pad_id,
+                                    int64_t N, int64_t d, int64_t V, float *dW, int accumulate, void *workspace,
+                                    size_t workspace_bytes, lce_stream_t stream) {
+    return emb_backward(dtype, dE, tokens, pad_id, N, d, V, dW, false, accumulate, workspace, workspace_bytes, stream);
+}
+
+lce_status_t lce_embedding_backward_bf16(lce_dtype_t dtype, const void *dE, const int64_t *tokens, int64_t pad_id,
+                                         int64_t N, int64_t d, int64_t V, void *dW, void *workspace,
+                                         size_t workspace_bytes, lce_stream_t stream) {
+    return emb_backward(dtype, dE, tokens, pad_id, N, d, V, dW, true, 0, workspace, workspace_bytes, stream);
 }
 
 size_t lce_workspace_size(int64_t N, int64_t d, int64_t V, lce_dtype_t dtype, int64_t vocab_chunk) {
@@ -1125,6 +1156,6 @@ lce_status_t lce_selftest_wait_timeout(int64_t cycles, int32_t *gave_up, lce_str
     return LCE_OK;
 }
 
-int lce_version(void) { return 500; }
+int lce_version(void) { return 600; }
 
 }  // extern "C"

@@ -260,26 +260,34 @@ __device__ __forceinline__ int emb_run_start(const int *keys, int j, int lo) {
 // of the chunk, when its segment continues into the chunk before / after,
 // into partial row 2c / 2c + 1.
 constexpr int kEmbRowsInFlight = 8;
+
+// Four columns of a dW row: fp32, or bf16 rounded to nearest from the fp32
+// sum (then written once, never accumulated into).
+__device__ __forceinline__ void emb_store4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ void emb_store4(__nv_bfloat16 *p, float4 v) {
+    reinterpret_cast<__nv_bfloat162 *>(p)[0] = __floats2bfloat162_rn(v.x, v.y);
+    reinterpret_cast<__nv_bfloat162 *>(p)[1] = __floats2bfloat162_rn(v.z, v.w);
+}
+
+template <typename O>
 __device__ __forceinline__ void emb_flush(const int *keys, int nv, int c, int j0, int j1, int r0, int r1, int key,
-                                          const float *acc, float4 wcur, int d, int col, float *dW, float *partial,
+                                          const float *acc, float4 wcur, int d, int col, O *dW, float *partial,
                                           int accumulate) {
     const bool before = r0 == j0 && j0 > 0 && keys[j0 - 1] == key;
     const bool after = r1 == j1 && j1 < nv && keys[j1] == key;
     float4 v = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    float *out;
     if (!before && !after) {
-        out = dW + static_cast<int64_t>(key) * d + col;
         if (accumulate) v.x += wcur.x, v.y += wcur.y, v.z += wcur.z, v.w += wcur.w;
+        emb_store4(dW + static_cast<int64_t>(key) * d + col, v);
     } else {
-        out = partial + static_cast<int64_t>(2 * c + (r0 == j0 ? 0 : 1)) * d + col;
+        emb_store4(partial + static_cast<int64_t>(2 * c + (r0 == j0 ? 0 : 1)) * d + col, v);
     }
-    *reinterpret_cast<float4 *>(out) = v;
 }
 
-template <typename T>
+template <typename T, typename O>
 __global__ void __launch_bounds__(64, 8)
     k_emb_segsum(const T *__restrict__ dE, const int *__restrict__ counts, const int *__restrict__ keys,
-                 const int *__restrict__ order, int d, float *__restrict__ dW, float *__restrict__ partial,
+                 const int *__restrict__ order, int d, O *__restrict__ dW, float *__restrict__ partial,
                  int accumulate) {
     const int nv = counts[0];
     const int nchunks = (nv + kEmbChunk - 1) / kEmbChunk;
@@ -302,8 +310,10 @@ __global__ void __launch_bounds__(64, 8)
             for (int r = 0; r < kEmbRowsInFlight; ++r) {
                 const int j = jb + r;
                 const bool starts = j < j1 && kk[r] != (r ? kk[r - 1] : key);
-                pre[r] = (accumulate && starts) ? *reinterpret_cast<const float4 *>(dW + static_cast<int64_t>(kk[r]) * d + col)
-                                                : zero4;
+                pre[r] = (accumulate && starts)
+                             ? *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(dW) +
+                                                                 static_cast<int64_t>(kk[r]) * d + col)
+                             : zero4;
                 if (j < j1) {
                     Vec4<T>::load(dE + static_cast<int64_t>(order[j]) * d + col, x[r]);
                 } else {
@@ -334,8 +344,9 @@ __global__ void __launch_bounds__(64, 8)
 // segment, in chunk order, into dW[token]. The block's 64 threads test 64
 // chunk boundaries at once to find how far the segment reaches, then each
 // thread loads its columns of those partial rows with eight loads in flight.
+template <typename O>
 __global__ void __launch_bounds__(64, 8)
-    k_emb_combine(const int *__restrict__ counts, const int *__restrict__ keys, int d, float *__restrict__ dW,
+    k_emb_combine(const int *__restrict__ counts, const int *__restrict__ keys, int d, O *__restrict__ dW,
                   const float *__restrict__ partial, int accumulate) {
     const int nv = counts[0];
     const int nchunks = (nv + kEmbChunk - 1) / kEmbChunk;
@@ -358,9 +369,9 @@ __global__ void __launch_bounds__(64, 8)
             if (n < static_cast<int>(blockDim.x)) break;
         }
         if (!active) continue;
-        float *out = dW + static_cast<int64_t>(key) * d + col;
+        O *out = dW + static_cast<int64_t>(key) * d + col;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        if (accumulate) {
+        if (accumulate) {   // fp32 dW only
             const float4 a = *reinterpret_cast<const float4 *>(out);
             acc[0] = a.x, acc[1] = a.y, acc[2] = a.z, acc[3] = a.w;
         }
@@ -379,7 +390,7 @@ __global__ void __launch_bounds__(64, 8)
             for (int q = 0; q < 8; ++q)
                 if (q0 + q <= len) acc[0] += v[q].x, acc[1] += v[q].y, acc[2] += v[q].z, acc[3] += v[q].w;
         }
-        *reinterpret_cast<float4 *>(out) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        emb_store4(out, make_float4(acc[0], acc[1], acc[2], acc[3]));
     }
 }
 

@@ -318,8 +318,9 @@ def embedding_workspace_size(N: int, d: int) -> int:
 
 def embedding_backward(dE, tokens, pad_id: int, V: int, *, dW=None, accumulate: bool = False, workspace=None,
                        stream=None):
-    """dW [V, d] fp32 with each token's gradient rows summed in a fixed order
-    (overwritten, or added into a given dW with accumulate). `workspace`: a
+    """dW [V, d] with each token's gradient rows summed in fp32 in a fixed
+    order: fp32 (overwritten, or added into a given dW with accumulate), or a
+    given bf16 dW (each row sum rounded once; overwritten). `workspace`: a
     uint8 CUDA tensor of at least embedding_workspace_size(N, d) bytes; without
     it the library allocates its scratch on the stream."""
     if not (dE.is_cuda and tokens.is_cuda) or dE.dtype not in _DT or tokens.dtype != torch.int64:
@@ -330,13 +331,21 @@ def embedding_backward(dE, tokens, pad_id: int, V: int, *, dW=None, accumulate: 
     if dW is None:
         dW = torch.empty((V, dE.shape[1]), dtype=torch.float32, device=dE.device)
         accumulate = False
-    elif dW.dtype != torch.float32 or dW.shape != (V, dE.shape[1]) or not dW.is_contiguous():
-        raise ValueError("dW must be a contiguous fp32 [V, d] tensor")
+    elif dW.dtype not in (torch.float32, torch.bfloat16) or dW.shape != (V, dE.shape[1]) or not dW.is_contiguous():
+        raise ValueError("dW must be a contiguous fp32 (or bf16) [V, d] tensor")
+    if dW.dtype == torch.bfloat16 and accumulate:
+        raise ValueError("a bf16 dW is overwritten, not accumulated into")
     ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel()) if workspace is not None else (None, 0)
-    _abi.check(_abi.lib().lce_embedding_backward(_DT[dE.dtype], dE.data_ptr(), tokens.data_ptr(), int(pad_id),
-                                                 tokens.shape[0], dE.shape[1], V, dW.data_ptr(),
-                                                 1 if accumulate else 0, ws_ptr, ws_bytes, _stream(stream)),
-               "lce_embedding_backward")
+    if dW.dtype == torch.bfloat16:
+        _abi.check(_abi.lib().lce_embedding_backward_bf16(_DT[dE.dtype], dE.data_ptr(), tokens.data_ptr(),
+                                                          int(pad_id), tokens.shape[0], dE.shape[1], V,
+                                                          dW.data_ptr(), ws_ptr, ws_bytes, _stream(stream)),
+                   "lce_embedding_backward_bf16")
+    else:
+        _abi.check(_abi.lib().lce_embedding_backward(_DT[dE.dtype], dE.data_ptr(), tokens.data_ptr(), int(pad_id),
+                                                     tokens.shape[0], dE.shape[1], V, dW.data_ptr(),
+                                                     1 if accumulate else 0, ws_ptr, ws_bytes, _stream(stream)),
+                   "lce_embedding_backward")
     return dW
 
 
@@ -350,8 +359,10 @@ class _Embedding(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dE):
         (tokens,) = ctx.saved_tensors
-        dW = embedding_backward(dE.to(ctx.w_dtype).contiguous(), tokens, ctx.pad_id, ctx.V)
-        return dW.to(ctx.w_dtype), None, None
+        # the gradient of W in W's dtype, written by the library from dE as it
+        # arrives (bf16 or fp32)
+        dW = torch.empty((ctx.V, dE.shape[1]), dtype=ctx.w_dtype, device=dE.device)
+        return embedding_backward(dE, tokens, ctx.pad_id, ctx.V, dW=dW), None, None
 
 
 def embedding(W, tokens, pad_id: int = 0):

@@ -328,6 +328,17 @@ lce_status_t lce_embedding_backward(lce_dtype_t dtype, const void *dE, const int
                                     int64_t N, int64_t d, int64_t V, float *dW, int accumulate, void *workspace,
                                     size_t workspace_bytes, lce_stream_t stream);
 
+/*
+ * The same gradient written as bf16 [V,d] (dW, device, 16-byte aligned):
+ * every row sum is taken in fp32 exactly as above and rounded to nearest once
+ * when it is stored, so the result equals lce_embedding_backward's fp32 dW
+ * rounded to bf16. For a bf16 W whose gradient is kept in its own dtype; dW
+ * is overwritten (no accumulation: a second rounding would follow).
+ */
+lce_status_t lce_embedding_backward_bf16(lce_dtype_t dtype, const void *dE, const int64_t *tokens, int64_t pad_id,
+                                         int64_t N, int64_t d, int64_t V, void *dW, void *workspace,
+                                         size_t workspace_bytes, lce_stream_t stream);
+
 /* ABI version: major*10000 + minor*100 + patch. */
 int lce_version(void);
 

@@ -68,7 +68,7 @@ def test_host_checks_without_gpu(lib):
     a.accumulate_dW, a.token_chunk = 0, 4
     assert lib.lce_run(ctypes.byref(a)) == 10          # bf16 dW over token chunks
     assert lib.lce_status_string(0) == b"ok"
-    assert lib.lce_version() == 500          # 0.5.0: bf16 dW output
+    assert lib.lce_version() == 600          # 0.6.0: bf16 embedding gradient
 
 
 def test_workspace_size_is_linear_in_N_not_N_times_V(lib):

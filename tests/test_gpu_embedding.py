@@ -121,6 +121,37 @@ def test_embedding_autograd_function():
     np.testing.assert_array_equal(np64(E.detach()), oracle.embedding_forward(W, t, 0))
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["dE_bf16", "dE_fp32"])
+@pytest.mark.parametrize("shape", [(1, 8, 3, 0), (777, 200, 5000, 0), (4100, 256, 300, 2), (3000, 64, 40, 1)],
+                         ids=lambda s: f"N{s[0]}_d{s[1]}_V{s[2]}_pad{s[3]}")
+def test_embedding_backward_bf16_output_is_the_fp32_output_rounded(shape, dtype):
+    """bf16 dW: every row sum taken in fp32 as for the fp32 output and rounded
+    once (tokens whose rows span several 32-element chunks included: V = 40
+    and 300 with thousands of positions), bit for bit."""
+    N, d, V, pad = shape
+    _, _, _, _, dEd, td = _case(N, d, V, pad, dtype, seed=7)
+    dW32 = lce.embedding_backward(dEd, td, pad, V)
+    dW16 = torch.full((V, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lce.embedding_backward(dEd, td, pad, V, dW=dW16)
+    torch.cuda.synchronize()
+    assert lce.device_status() == 0
+    assert torch.equal(dW16.view(torch.int16), dW32.to(torch.bfloat16).view(torch.int16))
+    with pytest.raises(ValueError):
+        lce.embedding_backward(dEd, td, pad, V, dW=dW16, accumulate=True)
+
+
+def test_embedding_autograd_bf16_W_grad_in_bf16():
+    W, dE, t, Wd, dEd, td = _case(900, 96, 700, 0, torch.bfloat16, seed=5)
+    Wp = Wd.clone().requires_grad_(True)
+    E = lce.embedding(Wp, td, 0)
+    E.backward(dEd)
+    torch.cuda.synchronize()
+    assert Wp.grad.dtype == torch.bfloat16
+    ref32 = lce.embedding_backward(dEd, td, 0, 700)
+    assert torch.equal(Wp.grad.view(torch.int16), ref32.to(torch.bfloat16).view(torch.int16))
+    assert rel_fro(np64(Wp.grad), oracle.embedding_backward(dE, t, 0, 700)) <= 2 ** -8
+
+
 def test_embedding_llama8b_shape_sampled_rows():
     """Full llama8b shape (N=16384, d=4096, V=128256): Zipf token ids with the
     workload's padding; the gradient checked on 256 sampled vocab rows (the
