@@ -964,17 +964,18 @@ lce_status_t emb_backward(lce_dtype_t dtype, const void *dE, const int64_t *toke
     const int *skeys = keys[(passes - 1) & 1];
     const int *order = vals[(passes - 1) & 1];
     const unsigned slices = static_cast<unsigned>((d + kEmbSegCols - 1) / kEmbSegCols);
+    const unsigned sum_slices = static_cast<unsigned>((d + kEmbSegSumCols - 1) / kEmbSegSumCols);
     const int64_t cmax = emb_chunks_max(N);
-    const dim3 pgrid(static_cast<unsigned>(cmax < 8 * di->sms ? cmax : 8 * di->sms), slices);
+    const dim3 pgrid(static_cast<unsigned>(cmax < 8 * di->sms ? cmax : 8 * di->sms), sum_slices);
     const int acc = accumulate ? 1 : 0;
     const int di32 = static_cast<int>(d);
     auto segsum = [&](auto *out) {
         using O = std::remove_pointer_t<decltype(out)>;
         if (dtype == LCE_BF16)
-            k_emb_segsum<__nv_bfloat16, O><<<pgrid, kEmbSegCols / 4, 0, st>>>(
+            k_emb_segsum<__nv_bfloat16, O><<<pgrid, kEmbSegSumCols / 8, 0, st>>>(
                 static_cast<const __nv_bfloat16 *>(dE), counts, skeys, order, di32, out, partial, acc);
         else
-            k_emb_segsum<float, O><<<pgrid, kEmbSegCols / 4, 0, st>>>(static_cast<const float *>(dE), counts, skeys,
+            k_emb_segsum<float, O><<<pgrid, kEmbSegSumCols / 8, 0, st>>>(static_cast<const float *>(dE), counts, skeys,
                                                                       order, di32, out, partial, acc);
     };
     const dim3 cgrid(static_cast<unsigned>(cmax < 4 * di->sms ? cmax : 4 * di->sms), slices);

@@ -36,7 +36,7 @@ constexpr int kEmbSortThreads = 1024;   // threads per sort block: one element e
 constexpr int kEmbRadixBits = 9;
 constexpr int kEmbBuckets = 1 << kEmbRadixBits;
 constexpr int kEmbMaxSortBlocks = 64;
-constexpr int kEmbSegCols = 256;   // columns per segment-sum block (64 threads x 4)
+constexpr int kEmbSegCols = 256;   // columns per combine block (64 threads x 4)
 constexpr int kEmbChunk = 32;      // sorted elements per segment-sum chunk
 
 // Sort geometry for N positions: blocks and the elements each block covers
@@ -251,36 +251,54 @@ __device__ __forceinline__ int emb_run_start(const int *keys, int j, int lo) {
     return j;
 }
 
-// Per (32-element chunk, 256-column slice): the sum of each run of equal
-// tokens in order, four columns per thread. The chunk's rows are loaded
-// eight at a time whatever the run boundaries (short runs are the common
-// case), together with dW's current value for every run that starts among
-// them (when accumulating), so that a batch costs one round trip to memory.
-// A run that is its token's whole segment goes into dW; the first / last run
-// of the chunk, when its segment continues into the chunk before / after,
-// into partial row 2c / 2c + 1.
-constexpr int kEmbRowsInFlight = 8;
+// Per (32-element chunk, 512-column slice): the sum of each run of equal
+// tokens in order, eight columns per thread (one 16-byte load per bf16 row).
+// The chunk's rows are loaded four at a time whatever the run boundaries
+// (short runs are the common case), together with dW's current value for
+// every run that starts among them (when accumulating), so that a batch
+// costs one round trip to memory. A run that is its token's whole segment
+// goes into dW; the first / last run of the chunk, when its segment continues
+// into the chunk before / after, into partial row 2c / 2c + 1.
+constexpr int kEmbRowsInFlight = 4;
+constexpr int kEmbSegSumCols = 512;   // columns per segment-sum block (64 threads x 8)
 
-// Four columns of a dW row: fp32, or bf16 rounded to nearest from the fp32
-// sum (then written once, never accumulated into).
-__device__ __forceinline__ void emb_store4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
-__device__ __forceinline__ void emb_store4(__nv_bfloat16 *p, float4 v) {
-    reinterpret_cast<__nv_bfloat162 *>(p)[0] = __floats2bfloat162_rn(v.x, v.y);
-    reinterpret_cast<__nv_bfloat162 *>(p)[1] = __floats2bfloat162_rn(v.z, v.w);
+// Eight columns of a dW or partial row: fp32, or bf16 rounded to nearest
+// from the fp32 sum (then written once, never accumulated into).
+__device__ __forceinline__ void emb_store8(float *p, const float *v) {
+    reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+    reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+__device__ __forceinline__ void emb_store8(__nv_bfloat16 *p, const float *v) {
+    __nv_bfloat162 h[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) h[k] = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+    *reinterpret_cast<uint4 *>(p) = *reinterpret_cast<const uint4 *>(h);
+}
+__device__ __forceinline__ void emb_load8(const __nv_bfloat16 *p, float *x) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) x[2 * k] = __uint_as_float(w[k] << 16), x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+}
+__device__ __forceinline__ void emb_load8(const float *p, float *x) {
+    const float4 a = reinterpret_cast<const float4 *>(p)[0], b = reinterpret_cast<const float4 *>(p)[1];
+    x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
 }
 
 template <typename O>
 __device__ __forceinline__ void emb_flush(const int *keys, int nv, int c, int j0, int j1, int r0, int r1, int key,
-                                          const float *acc, float4 wcur, int d, int col, O *dW, float *partial,
+                                          float *acc, const float *wcur, int d, int col, O *dW, float *partial,
                                           int accumulate) {
     const bool before = r0 == j0 && j0 > 0 && keys[j0 - 1] == key;
     const bool after = r1 == j1 && j1 < nv && keys[j1] == key;
-    float4 v = make_float4(acc[0], acc[1], acc[2], acc[3]);
     if (!before && !after) {
-        if (accumulate) v.x += wcur.x, v.y += wcur.y, v.z += wcur.z, v.w += wcur.w;
-        emb_store4(dW + static_cast<int64_t>(key) * d + col, v);
+        if (accumulate) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[k] += wcur[k];
+        }
+        emb_store8(dW + static_cast<int64_t>(key) * d + col, acc);
     } else {
-        emb_store4(partial + static_cast<int64_t>(2 * c + (r0 == j0 ? 0 : 1)) * d + col, v);
+        emb_store8(partial + static_cast<int64_t>(2 * c + (r0 == j0 ? 0 : 1)) * d + col, acc);
     }
 }
 
@@ -291,33 +309,35 @@ __global__ void __launch_bounds__(64, 8)
                  int accumulate) {
     const int nv = counts[0];
     const int nchunks = (nv + kEmbChunk - 1) / kEmbChunk;
-    const int col = blockIdx.y * kEmbSegCols + threadIdx.x * 4;
+    const int col = blockIdx.y * kEmbSegSumCols + threadIdx.x * 8;   // d % 8 == 0: all eight inside d
     if (col >= d) return;
-    const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int c = blockIdx.x; c < nchunks; c += gridDim.x) {
         const int j0 = c * kEmbChunk;
         const int j1 = j0 + kEmbChunk < nv ? j0 + kEmbChunk : nv;
         int key = -1, r0 = j0;
-        float4 wcur = zero4;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float wcur[8], acc[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) wcur[k] = acc[k] = 0.f;
         for (int jb = j0; jb < j1; jb += kEmbRowsInFlight) {
-            float x[kEmbRowsInFlight][4];
+            float x[kEmbRowsInFlight][8], pre[kEmbRowsInFlight][8];
             int kk[kEmbRowsInFlight];
-            float4 pre[kEmbRowsInFlight];
 #pragma unroll
             for (int r = 0; r < kEmbRowsInFlight; ++r) kk[r] = jb + r < j1 ? keys[jb + r] : -1;
 #pragma unroll
             for (int r = 0; r < kEmbRowsInFlight; ++r) {
                 const int j = jb + r;
                 const bool starts = j < j1 && kk[r] != (r ? kk[r - 1] : key);
-                pre[r] = (accumulate && starts)
-                             ? *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(dW) +
-                                                                 static_cast<int64_t>(kk[r]) * d + col)
-                             : zero4;
-                if (j < j1) {
-                    Vec4<T>::load(dE + static_cast<int64_t>(order[j]) * d + col, x[r]);
+                if (accumulate && starts) {
+                    emb_load8(reinterpret_cast<const float *>(dW) + static_cast<int64_t>(kk[r]) * d + col, pre[r]);
                 } else {
-                    x[r][0] = x[r][1] = x[r][2] = x[r][3] = 0.f;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) pre[r][k] = 0.f;
+                }
+                if (j < j1) {
+                    emb_load8(dE + static_cast<int64_t>(order[j]) * d + col, x[r]);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) x[r][k] = 0.f;
                 }
             }
 #pragma unroll
@@ -326,17 +346,24 @@ __global__ void __launch_bounds__(64, 8)
                 if (j >= j1) break;
                 if (kk[r] != key) {   // a run starts here; the one before (if any) is complete
                     if (j > j0) emb_flush(keys, nv, c, j0, j1, r0, j, key, acc, wcur, d, col, dW, partial, accumulate);
-                    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) acc[k] = 0.f, wcur[k] = pre[r][k];
                     r0 = j;
                     key = kk[r];
-                    wcur = pre[r];
                 }
 #pragma unroll
-                for (int k = 0; k < 4; ++k) acc[k] += x[r][k];
+                for (int k = 0; k < 8; ++k) acc[k] += x[r][k];
             }
         }
         emb_flush(keys, nv, c, j0, j1, r0, j1, key, acc, wcur, d, col, dW, partial, accumulate);
     }
+}
+
+// Four columns of a dW row (see emb_store8).
+__device__ __forceinline__ void emb_store4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ void emb_store4(__nv_bfloat16 *p, float4 v) {
+    reinterpret_cast<__nv_bfloat162 *>(p)[0] = __floats2bfloat162_rn(v.x, v.y);
+    reinterpret_cast<__nv_bfloat162 *>(p)[1] = __floats2bfloat162_rn(v.z, v.w);
 }
 
 // Segments that span chunks: the chunk holding a segment's first run adds
