@@ -19,10 +19,11 @@
 // offset; sub-chunks in order). The first pass reads the token ids directly
 // and drops padding and out-of-range ids, so no separate compaction runs.
 // The sorted list is then cut into fixed 32-element chunks: k_emb_segsum
-// sums, per chunk and 256-column slice, each run of equal tokens in order,
+// sums, per chunk and 512-column slice, each run of equal tokens in order,
 // straight into dW when the run is the token's whole segment, else into the
-// run's partial row; k_emb_combine adds the partial rows of each segment that
-// spans chunks, in chunk order, into dW.
+// run's partial row; k_emb_combine (256-column slices) adds the partial rows
+// of each segment that spans chunks, in chunk order, into dW. dW is fp32, or
+// bf16 with every fp32 row sum rounded once as it is stored.
 #pragma once
 
 #include <cuda_bf16.h>
