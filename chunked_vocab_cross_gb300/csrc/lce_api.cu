@@ -603,7 +603,7 @@ lce_status_t run_rows(const lce_args_t *a, const DevInfo &di, uint8_t *base, con
                 g.vlenw = chunk_len(cw);
             }
             g.mn3d = 1 | (mn3d_d ? 6 : 0);
-            g.dW = a->dW;
+            g.dW = static_cast<float *>(a->dW);   // bf16 rows when dw_bf16
             g.dw_bf16 = a->dW_bf16 ? 1 : 0;
             g.acc_dw = ctx.acc_dw ? 1 : 0;
             g.dH_acc = dHacc;

@@ -168,8 +168,8 @@ typedef struct {
     int64_t N, d, V;
     float *loss;              /* device fp32 scalar; required unless lse_in is given */
     void *dH;                 /* [N,d] of dtype, or NULL for forward only */
-    float *dW;                /* [V,d] fp32, or NULL for forward only (NULL iff dH is NULL, except that
-                                 dW is NULL with a fused optimizer) */
+    void *dW;                 /* [V,d] fp32 (bf16 with dW_bf16), or NULL for forward only (NULL iff dH
+                                 is NULL, except that dW is NULL with a fused optimizer) */
     int accumulate_dW;        /* nonzero: dW += gradient; zero: dW = gradient */
     float grad_scale;         /* multiplies dH and dW (0 is read as 1) */
     float *lse;               /* optional [N] fp32: per-row logsumexp (natural log), NaN on ignored rows */
