@@ -69,6 +69,32 @@ def test_reference_arm_other_ranks_exit_silently():
     assert r.returncode == 0 and r.stdout.strip() == ""
 
 
+def test_reference_arm_prints_one_contract_line():
+    """The reference arm (the C++ oracle on the host cores) prints one JSON
+    line with the contract's keys: metric, value, unit, the timed step,
+    cpu_baseline with the thread count, and an e2e object with no copies."""
+    env = dict(os.environ, LCE_REF_STEP_S="0.2")
+    env.pop("RANK", None)
+    env.pop("WORLD_SIZE", None)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "tiny",
+                        "--steps", "2", "--warmup", "1"], env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench_metric() and d["unit"] == "valid tokens/s"
+    assert d["value"] > 0 and d["ms_per_step"] > 0 and d["steps"] == 2 and d["warmup"] == 1
+    assert d["higher_is_better"] is True and d["dtype"] == "f64"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def bench_metric():
+    import bench
+    return bench.METRIC
+
+
 def test_kernel_hash_ignores_comments_only():
     import bench
     base = bench.kernel_src_sha256(["int a = 1;\nint b = a; // trailing\n", "asm(\"mov\");\n"])
