@@ -421,6 +421,62 @@ def eager_context(H, W, t, nv, steps):
                     "materialises N x V logits; context, not this path"}
 
 
+def cublas_context(H, W, t, nv, reps=5):
+    """Context only: the three contractions of the step as plain cuBLAS bf16
+    GEMMs on the valid rows (torch.matmul, materialised outputs): logits
+    Hc @ W^T [Nv, V], dH = G @ W [Nv, d] and dW = G^T @ Hc [V, d] for a bf16
+    G [Nv, V]. Each timed alone with CUDA events (median of `reps` after two
+    warm-ups); the library runs these three plus the logits recomputation
+    (four contractions of 2*Nv*d*V FLOPs). None if it does not fit."""
+    import torch
+    try:
+        Hc = H[t != -100].contiguous()
+        G = (torch.randn(Hc.shape[0], W.shape[0], device=H.device) * 1e-6).to(H.dtype)
+        out = {}
+        for name, fn in (("logits", lambda: Hc @ W.t()), ("dH", lambda: G @ W), ("dW", lambda: G.t() @ Hc)):
+            for _ in range(2):
+                fn()
+            times = []
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1))
+            out[name + "_ms"] = float(np.median(times))
+        flops = 2.0 * Hc.shape[0] * H.shape[1] * W.shape[0]
+        out["tflops_each"] = {k[:-3]: flops / (v / 1e3) / 1e12 for k, v in list(out.items())}
+        # the four contractions this path executes per step (logits twice, dH,
+        # dW) back to back, as long a run as the timed steps: the rate under
+        # the same power cap
+        def four():
+            Hc @ W.t()
+            Hc @ W.t()
+            G @ W
+            G.t() @ Hc
+        for _ in range(2):
+            four()
+        n = 10
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            four()
+        e1.record()
+        torch.cuda.synchronize()
+        out["four_contractions_ms"] = e0.elapsed_time(e1) / n
+        out["four_contractions_tflops"] = 4 * flops / (out["four_contractions_ms"] / 1e3) / 1e12
+        out["what"] = ("cuBLAS bf16 GEMMs of the same shapes with materialised outputs: each alone (median of "
+                       "5, burst), and the four this path executes per step (logits twice, dH, dW) back to back "
+                       "over 10 steps; context only")
+        del Hc, G
+        return out
+    except torch.cuda.OutOfMemoryError:
+        return None
+    finally:
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -622,6 +678,7 @@ def main():
         return
 
     context = None if args.no_context else eager_context(H, W, t, nv, args.steps)
+    cublas = None if args.no_context else cublas_context(H, W, t, nv)
 
     peaks, peak_src = load_peaks()
     useful_flops = 6.0 * nv * w.d * w.V
@@ -691,6 +748,7 @@ def main():
         "token_chunk": args.token_chunk or None,
         "logits_bytes_avoided": int(w.N * w.V * 4),
         "context_torch_eager": context,
+        "context_cublas_gemms": cublas,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
